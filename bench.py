@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark: GDN tail-replay state rebuild on GB300 (one rank per GPU).
+
+A step is one gdn_replay call over one layer's replay batch (default: one
+3277-token tail, 16 q/k heads shared by 32 v heads, d_k = d_v = 128, bf16
+inputs, fp32 state) with its inputs resident in HBM.  Prints one JSON line
+(rank 0).  ``--impl reference`` times the fp64 CPU oracle on the host cores
+instead, on a bounded sample of the same workload.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launch stream; a 256 MiB memset flushes L2 between steps (outside the
+events); a barrier and a device synchronize bracket the whole timed loop;
+the reported time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN tail-replay tokens/s per layer; state-rebuild us @3.2K tail; % roofline"
+CHUNK = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_r3277",
+                    choices=["layer_r3277", "layer_r1638", "varlen", "full_32k", "tiny"])
+    ap.add_argument("--precise", action="store_true", help="bf16 inputs on the fp32 CUDA-core path")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- workload
+
+def make_inputs(name: str, layer: int = 0):
+    from gated_deltanet_state_chunked_gb300 import synthetic
+    if name == "varlen":
+        return synthetic.varlen_workload_inputs(layer)
+    return synthetic.workload_inputs(name, layer)
+
+
+def describe(name, x):
+    lens = np.diff(x.cu_seqlens)
+    return {
+        "workload": name,
+        "tails": int(x.n_seqs), "tokens": int(x.total_tokens),
+        "tail_len_min": int(lens.min()) if len(lens) else 0, "tail_len_max": int(lens.max()) if len(lens) else 0,
+        "h_k": x.h_k, "h_v": x.h_v, "d_k": x.d_k, "d_v": x.d_v,
+        "inputs": x.dtype, "state": "f32", "S0": "zero", "chunk": CHUNK,
+        "l2_flush": "256 MiB memset between timed steps",
+    }
+
+
+def algorithmic(x, with_O=True):
+    """Algorithmic FLOPs and HBM bytes of one replay launch (fixed formulas)."""
+    T, Hk, Hv, dk, dv, N = x.total_tokens, x.h_k, x.h_v, x.d_k, x.d_v, x.n_seqs
+    e = 2 if x.dtype == "bf16" else 4
+    flops = T * Hv * (6 * dk * dv + CHUNK * (6 * dk + 4 * dv))
+    per_tok = 2 * Hk * dk * e + Hv * dv * e + 8 * Hv + (Hv * dv * e if with_O else 0)
+    byts = T * per_tok + N * Hv * dv * dk * 4 + 4 * (N + 1)
+    return flops, byts
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_state_chunked_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        m = re.match(r"\s*traffic\s+workload=(\S+)\s+sources=(\w+)\s+bytes_per_launch=(\d+)", line)
+        if m and m.group(1) == workload and m.group(2) == source_digest():
+            return int(m.group(3))
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(x, budget_s: float, max_reps: int = 50):
+    """Time the fp64 oracle on a bounded sample of one layer's replay batch:
+    whole (tail, head) problems, as many as fit in about budget_s.  Returns
+    (tokens/s per layer, seconds, threads, sample description)."""
+    import oracle
+    pairs = [(s, h) for s in range(x.n_seqs) for h in range(x.h_v)]
+    lens = np.diff(x.cu_seqlens)
+    threads = oracle.num_threads()
+    # probe with one problem per thread to estimate the rate
+    probe = pairs[: max(1, min(len(pairs), threads))]
+    t0 = time.perf_counter()
+    oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, want_O=True, sel=probe)
+    dt = time.perf_counter() - t0
+    per_pair = dt / len(probe) * min(threads, len(probe))  # wall time per problem-wave slot
+    n_fit = int(max(1, budget_s / max(per_pair, 1e-6) * threads))
+    sample = pairs[: min(len(pairs), n_fit)]
+    reps, total, t_start = 0, 0.0, time.perf_counter()
+    while reps < max_reps:
+        t0 = time.perf_counter()
+        oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, want_O=True, sel=sample)
+        total += time.perf_counter() - t0
+        reps += 1
+        if time.perf_counter() - t_start >= budget_s * 0.5 or len(sample) < len(pairs):
+            break
+    head_tokens = sum(int(lens[s]) for s, _ in sample) * reps
+    tokens_per_layer = head_tokens / x.h_v  # a layer's token covers h_v heads
+    desc = (f"{len(sample)} of {len(pairs)} (tail, v-head) replays x {reps} rep(s), full fp64 token loop "
+            f"with outputs; tokens/s per layer = tail tokens x heads sampled / h_v / time")
+    return tokens_per_layer / total, total, threads, desc
+
+
+# ----------------------------------------------------------------------------- runs
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    x = make_inputs(args.workload)
+    steps = []
+    for i in range(args.warmup + args.steps):
+        v, secs, threads, desc = time_oracle(x, budget_s=3.0, max_reps=1)
+        if i >= args.warmup:
+            steps.append((v, secs))
+    value = statistics.mean(v for v, _ in steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(s for _, s in steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(args.workload, x),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from gated_deltanet_state_chunked_gb300 import _lib, api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _lib.load()
+    x = make_inputs(args.workload, layer=rank)  # each rank replays its own layer's batch
+    dt = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+
+    def dtens(a, d):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(d)
+
+    q, k, v = dtens(x.q, dt), dtens(x.k, dt), dtens(x.v, dt)
+    g, beta = dtens(x.g, torch.float32), dtens(x.beta, torch.float32)
+    cu = dtens(x.cu_seqlens, torch.int32)
+    T, n = x.total_tokens, x.n_seqs
+    O = torch.empty((T, x.h_v, x.d_v), dtype=dt, device=dev)
+    S = torch.empty((n, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.gdn_replay(q, k, v, g, beta, cu, None, O_out=O, S_out=S, precise=args.precise, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    api.gdn_get_status()
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(dev.index)
+    sampler = ClockSampler(gpu_id)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    api.gdn_get_status()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # parity of the last timed step on a few sampled (tail, head) problems
+    import oracle
+    sel = [(0, 0), (0, x.h_v - 1), (x.n_seqs - 1, x.h_v // 2)] if rank == 0 else None
+    parity = None
+    if sel is not None:
+        S_ref, O_ref = oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, want_O=True, sel=sel)
+        Sh, Oh = S.cpu().double().numpy(), O.float().cpu().double().numpy()
+        es = max(oracle.rel_err(Sh[s, h], S_ref[s, h]) for s, h in sel)
+        rows = [(slice(int(x.cu_seqlens[s]), int(x.cu_seqlens[s + 1])), h) for s, h in sel]
+        eo = max(oracle.rel_err(Oh[r, h], O_ref[r, h]) for r, h in rows)
+        parity = {"rel_err_S_max": es, "rel_err_O_max": eo, "sampled": [list(p) for p in sel]}
+
+    # end to end through the public call with host buffers: H2D inputs, replay, D2H result
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory() for a in (x.q, x.k, x.v))
+        hg, hb = (torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in (x.g, x.beta))
+        hcu = torch.from_numpy(x.cu_seqlens.astype(np.int32)).pin_memory()
+        hO = torch.empty(O.shape, dtype=dt).pin_memory()
+        hS = torch.empty(S.shape, dtype=torch.float32).pin_memory()
+        dq, dk_, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dg, db, dcu = torch.empty_like(g), torch.empty_like(beta), torch.empty_like(cu)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hcu))
+        d2h = hO.numel() * hO.element_size() + hS.numel() * hS.element_size()
+
+        def e2e_step():
+            for dst, src in ((dq, hq), (dk_, hk), (dv, hv), (dg, hg), (db, hb), (dcu, hcu)):
+                dst.copy_(src, non_blocking=True)
+            api.gdn_replay(dq, dk_, dv, dg, db, dcu, None, O_out=O, S_out=S, precise=args.precise, stream=stream)
+            hO.copy_(O, non_blocking=True)
+            hS.copy_(S, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            flush.zero_()
+            e2e_step()
+        es_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee_ = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.zero_()
+            es_[i].record(stream)
+            e2e_step()
+            ee_[i].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = sum(a.elapsed_time(b) for a, b in zip(es_, ee_)) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, secs, threads, desc = time_oracle(x, budget_s=15.0)
+        cpu = {"value": v_cpu, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    flops, byts = algorithmic(x, with_O=True)
+    peaks, peak_src = load_peaks()
+    t_s = ms * 1e-3
+    gbs = byts / t_s / 1e9
+    tfs = flops / t_s / 1e12
+    traffic = recorded_traffic(args.workload)
+    roofline = {
+        "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+        "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+        else "fallback 6.8 TB/s",
+        "kernel": "gdn_replay (all launches of one call)", "algorithmic_bytes": byts, "algorithmic_flops": flops,
+        "tensor": {"achieved": tfs, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": tfs / peaks["bf16_tflops"]},
+    }
+    line = {
+        "metric": METRIC, "value": world * T / t_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "state_rebuild_us": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": x.dtype, "data": "synthetic",
+        "config": describe(args.workload, x) | {"path": "precise" if args.precise else "default",
+                                                "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * LAUNCHES_PER_CALL,
+        "clocks": clocks, "parity": parity,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# kernels one gdn_replay call launches (the L2 flush memset is torch's, not counted)
+LAUNCHES_PER_CALL = 1
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

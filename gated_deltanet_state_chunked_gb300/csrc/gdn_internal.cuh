@@ -1,0 +1,52 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;    // tokens per scan chunk
+constexpr int kMaxHead = 128; // largest d_k / d_v
+
+// Parameters of one replay (or chunk-operator) launch on the fp32 CUDA-core path.
+struct SimtParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const int32_t* cu;  // nullptr: one sequence of total_tokens
+  const float* S0;
+  void* O;
+  float* S_out;   // value rows: [n_seqs][h_v][d_v][d_k]
+  float* T_out;   // chunk-operator mode: [n_seqs][h_v][d_k][d_k]
+  int n_seqs, total_tokens, h_k, h_v, d_k, d_v;
+  int augmented;  // 1: state carries d_k extra transition rows (chunk operator)
+  int l2norm;
+  int write_O;
+  float scale;
+  int* status;    // sticky device status word
+};
+
+cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t stream);
+
+constexpr int kMaxCompose = 256;  // largest K of one gdn_compose call
+
+// Passed by value: the K device pointers travel in the kernel parameters.
+struct ComposeParams {
+  const float* T[kMaxCompose];
+  const float* Slocal[kMaxCompose];
+  const float* S_in;
+  float* S_out;
+  int K, h, d_k, d_v;
+};
+
+cudaError_t launch_compose_simt(const ComposeParams& p, cudaStream_t stream);
+
+// Sticky status word of the current device (device pointer).
+int* device_status_word();
+
+}  // namespace gdn

@@ -1,0 +1,309 @@
+// fp32 CUDA-core chunked scan: the precise path of gdn_replay (fp32 inputs,
+// or bf16 inputs with GDN_PRECISE) and the whole of gdn_chunk_operator.
+//
+// Method: "Tail-Replay: Escaping the Curse of Linear Attention in Prefix
+// Caching for Hybrid LLMs", section 2 Eq. (1) and section 3 Eq. (2), run
+// chunk by chunk.  Within a chunk of C = 64 tokens with inclusive gate sums
+// G_t (gamma_t = exp(G_t)) and entering state S0, unrolling Eq. (1) gives
+//     S_t = gamma_t S0 + sum_{s<=t} exp(G_t - G_s) u_s k_s^T,
+// where the corrected values u_s solve the unit lower-triangular system
+//     (I + A) U = diag(beta) (V - diag(gamma) K S0^T),
+//     A_ts = beta_t exp(G_t - G_s) k_t.k_s   (s < t).
+// Hence, with M = (I + A)^{-1}:
+//     U      = M diag(beta) (V - diag(gamma) K S0^T)
+//     S_end  = gamma_C S0 + U^T diag(exp(G_C - G_s)) K
+//     O      = diag(gamma) Q S0^T + (L o Q K^T) U,   L_ts = exp(G_t - G_s), s <= t.
+// Only S is carried from chunk to chunk, in fp32.
+//
+// Chunk-operator mode ("LinearKV: One Cached State Suffices for
+// Position-Independent Caching in Hybrid LLMs", composition passage): the
+// state gains d_k extra rows P, seeded with the identity and fed zero values.
+// Rows evolve independently, so after the chunk P = T_1 ... T_n
+// (right-multiplied form) = T_C^T, written transposed as T_C.
+//
+// One CTA owns a 32-row slice of one (sequence, v-head) state and walks its
+// chunks; the chunk-shared quantities (Gram matrices, M) are recomputed per
+// slice.  Partial last chunks are padded with tokens that have k = 0,
+// beta = 0, g = 0: identity transitions whose outputs are not stored.
+#include <cuda_bf16.h>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int C = kChunk;
+constexpr int RS = 32;                // state rows per CTA
+constexpr int KST = kMaxHead + 4;     // row stride of K/Q/S tiles (floats)
+constexpr int VST = RS + 1;           // row stride of V/R/U tiles
+constexpr int GST = C + 1;            // row stride of the 64x64 tiles
+constexpr int NT = 256;
+
+struct Smem {
+  float K[C * KST];
+  float Q[C * KST];
+  float S[RS * KST];
+  float V[C * VST];    // values, then R, then U
+  float A[C * GST];    // strictly lower A
+  float P[C * GST];    // (L o Q K^T), inclusive lower
+  float M[C * GST];    // (I + A)^{-1}
+  float X[C * VST];    // K S0^T
+  float G[C];          // inclusive gate sums
+  float gam[C];        // exp(G_t)
+  float wend[C];       // exp(G_last - G_t)
+  float beta[C];
+};
+
+__device__ __forceinline__ float ld_in(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_out(float* p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int slice = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int DK = p.d_k, DV = p.d_v;
+  const int rows_total = DV + (p.augmented ? DK : 0);
+  const int row0 = slice * RS;
+  const int hk = h / (p.h_v / p.h_k);
+  const Tin* __restrict__ q = static_cast<const Tin*>(p.q);
+  const Tin* __restrict__ k = static_cast<const Tin*>(p.k);
+  const Tin* __restrict__ v = static_cast<const Tin*>(p.v);
+
+  // cu == nullptr: a single sequence covering every token
+  const int t_begin = p.cu ? p.cu[seq] : 0;
+  const int t_end = p.cu ? p.cu[seq + 1] : p.total_tokens;
+  if (t_begin < 0 || t_end < t_begin || t_end > p.total_tokens) {
+    if (tid == 0) atomicExch(p.status, GDN_ERR_SHAPE);
+    return;
+  }
+
+  // entering state of this slice
+  for (int i = tid; i < RS * DK; i += NT) {
+    const int r = i / DK, d = i % DK, rg = row0 + r;
+    float s = 0.f;
+    if (rg < DV) {
+      if (p.S0) s = p.S0[(((size_t)seq * p.h_v + h) * DV + rg) * DK + d];
+    } else if (rg < rows_total) {
+      s = (d == rg - DV) ? 1.f : 0.f;
+    }
+    sm.S[r * KST + d] = s;
+  }
+
+  for (int t0 = t_begin; t0 < t_end; t0 += C) {
+    const int n = min(C, t_end - t0);
+    __syncthreads();
+    // ---- load the chunk
+    for (int i = tid; i < C * DK; i += NT) {
+      const int t = i / DK, d = i % DK;
+      const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d;
+      sm.K[t * KST + d] = t < n ? ld_in(k, off) : 0.f;
+      if (p.write_O) sm.Q[t * KST + d] = t < n ? ld_in(q, off) : 0.f;
+    }
+    for (int i = tid; i < C * RS; i += NT) {
+      const int t = i / RS, r = i % RS, rg = row0 + r;
+      float x = 0.f;
+      if (t < n && rg < DV) x = ld_in(v, ((size_t)(t0 + t) * p.h_v + h) * DV + rg);
+      sm.V[t * VST + r] = x;
+    }
+    if (tid < C) {
+      const bool in = tid < n;
+      sm.G[tid] = in ? p.g[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
+      sm.beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
+    }
+    __syncthreads();
+
+    // ---- per-token L2 normalisation (and q scale), gate prefix sums
+    {
+      const int warp = tid / 32, lane = tid % 32;
+      for (int t = warp; t < C; t += NT / 32) {
+        float sk = 0.f, sq = 0.f;
+        for (int d = lane; d < DK; d += 32) {
+          const float a = sm.K[t * KST + d];
+          sk += a * a;
+          if (p.write_O) { const float b = sm.Q[t * KST + d]; sq += b * b; }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        }
+        const float fk = p.l2norm ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
+        const float fq = (p.l2norm ? 1.f / sqrtf(sq + 1e-6f) : 1.f) * p.scale;
+        for (int d = lane; d < DK; d += 32) {
+          sm.K[t * KST + d] *= fk;
+          if (p.write_O) sm.Q[t * KST + d] *= fq;
+        }
+      }
+      if (warp == 0) {
+        float a = sm.G[lane], b = sm.G[lane + 32];
+        for (int o = 1; o < 32; o <<= 1) {
+          const float xa = __shfl_up_sync(0xffffffffu, a, o);
+          const float xb = __shfl_up_sync(0xffffffffu, b, o);
+          if (lane >= o) { a += xa; b += xb; }
+        }
+        b += __shfl_sync(0xffffffffu, a, 31);
+        sm.G[lane] = a;
+        sm.G[lane + 32] = b;
+        sm.gam[lane] = expf(a);
+        sm.gam[lane + 32] = expf(b);
+        const float Gl = __shfl_sync(0xffffffffu, b, 31);
+        sm.wend[lane] = expf(Gl - a);
+        sm.wend[lane + 32] = expf(Gl - b);
+      }
+    }
+    __syncthreads();
+
+    // ---- Gram matrices: A (strictly lower, gated, beta-weighted) and P (inclusive lower, gated)
+    {
+      const int ti = (tid / 16) * 4, si = (tid % 16) * 4;
+      float akk[4][4] = {}, aqk[4][4] = {};
+      for (int d = 0; d < DK; ++d) {
+        float a[4], b[4], c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          a[i] = sm.K[(ti + i) * KST + d];
+          b[i] = sm.K[(si + i) * KST + d];
+          c[i] = p.write_O ? sm.Q[(ti + i) * KST + d] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            akk[i][j] = fmaf(a[i], b[j], akk[i][j]);
+            aqk[i][j] = fmaf(c[i], b[j], aqk[i][j]);
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int t = ti + i, s = si + j;
+          const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
+          sm.A[t * GST + s] = s < t ? sm.beta[t] * decay * akk[i][j] : 0.f;
+          sm.P[t * GST + s] = s <= t ? decay * aqk[i][j] : 0.f;
+        }
+    }
+    __syncthreads();
+
+    // ---- M = (I + A)^{-1} by forward substitution, one column per thread (warps 0-1);
+    //      meanwhile X = K S0^T (warps 2-7)
+    if (tid < C) {
+      const int j = tid;
+      for (int t = 0; t < C; ++t) {
+        float m;
+        if (t < j) m = 0.f;
+        else if (t == j) m = 1.f;
+        else {
+          float acc0 = 0.f, acc1 = 0.f;
+          int s = j;
+          for (; s + 1 < t; s += 2) {
+            acc0 = fmaf(sm.A[t * GST + s], sm.M[s * GST + j], acc0);
+            acc1 = fmaf(sm.A[t * GST + s + 1], sm.M[(s + 1) * GST + j], acc1);
+          }
+          if (s < t) acc0 = fmaf(sm.A[t * GST + s], sm.M[s * GST + j], acc0);
+          m = -(acc0 + acc1);
+        }
+        sm.M[t * GST + j] = m;
+      }
+    } else {
+      for (int i = tid - C; i < C * RS; i += NT - C) {
+        const int t = i / RS, r = i % RS;
+        float acc = 0.f;
+        for (int d = 0; d < DK; ++d) acc = fmaf(sm.K[t * KST + d], sm.S[r * KST + d], acc);
+        sm.X[t * VST + r] = acc;
+      }
+    }
+    __syncthreads();
+
+    // ---- R = diag(beta) (V - diag(gamma) X)   (in place in V)
+    for (int i = tid; i < C * RS; i += NT) {
+      const int t = i / RS, r = i % RS;
+      sm.V[t * VST + r] = sm.beta[t] * (sm.V[t * VST + r] - sm.gam[t] * sm.X[t * VST + r]);
+    }
+    __syncthreads();
+
+    // ---- U = M R   (into X, then copied back into V)
+    for (int i = tid; i < C * RS; i += NT) {
+      const int t = i / RS, r = i % RS;
+      float acc = 0.f;
+      for (int s = 0; s <= t; ++s) acc = fmaf(sm.M[t * GST + s], sm.V[s * VST + r], acc);
+      sm.X[t * VST + r] = acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < C * RS; i += NT) sm.V[(i / RS) * VST + (i % RS)] = sm.X[(i / RS) * VST + (i % RS)];
+    __syncthreads();
+
+    // ---- outputs O = diag(gamma) Q S0^T + P U, and the new state (into registers)
+    if (p.write_O) {
+      Tin* O = static_cast<Tin*>(p.O);
+      for (int i = tid; i < C * RS; i += NT) {
+        const int t = i / RS, r = i % RS, rg = row0 + r;
+        if (t >= n || rg >= DV) continue;
+        float acc = 0.f;
+        for (int d = 0; d < DK; ++d) acc = fmaf(sm.Q[t * KST + d], sm.S[r * KST + d], acc);
+        acc *= sm.gam[t];
+        for (int s = 0; s <= t; ++s) acc = fmaf(sm.P[t * GST + s], sm.V[s * VST + r], acc);
+        st_out(O, ((size_t)(t0 + t) * p.h_v + h) * DV + rg, acc);
+      }
+    }
+    constexpr int PER = RS * kMaxHead / NT;  // 16 state entries per thread
+    float snew[PER];
+    const float gC = sm.gam[C - 1];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int i = tid + e * NT;
+      const int r = i / kMaxHead, d = i % kMaxHead;
+      float acc = 0.f;
+      if (d < DK) {
+        acc = gC * sm.S[r * KST + d];
+        for (int t = 0; t < C; ++t) acc = fmaf(sm.wend[t] * sm.V[t * VST + r], sm.K[t * KST + d], acc);
+      }
+      snew[e] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int i = tid + e * NT;
+      const int r = i / kMaxHead, d = i % kMaxHead;
+      if (d < DK) sm.S[r * KST + d] = snew[e];
+    }
+  }
+  __syncthreads();
+
+  // ---- final state: value rows to S_out, transition rows (P = T_C^T) to T_out transposed
+  for (int i = tid; i < RS * DK; i += NT) {
+    const int r = i / DK, d = i % DK, rg = row0 + r;
+    const float s = sm.S[r * KST + d];
+    if (rg < DV) {
+      p.S_out[(((size_t)seq * p.h_v + h) * DV + rg) * DK + d] = s;
+    } else if (rg < rows_total) {
+      const int pr = rg - DV;  // P[pr][d] = T_C[d][pr]
+      p.T_out[(((size_t)seq * p.h_v + h) * DK + d) * DK + pr] = s;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t stream) {
+  if (p.n_seqs == 0) return cudaSuccess;
+  const int rows = p.d_v + (p.augmented ? p.d_k : 0);
+  dim3 grid((rows + RS - 1) / RS, p.h_v, p.n_seqs);
+  const size_t smem = sizeof(Smem);
+  cudaError_t e;
+  if (bf16) {
+    e = cudaFuncSetAttribute(simt_chunk_scan_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    simt_chunk_scan_kernel<__nv_bfloat16><<<grid, NT, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(simt_chunk_scan_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    simt_chunk_scan_kernel<float><<<grid, NT, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,157 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: the Gated DeltaNet tail-replay state rebuild
+ * on one GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * State layout.  A recurrent state S is fp32, d_v x d_k, row-major, and one
+ * token updates it as
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   alpha_t = exp(g_t),
+ * which is Eq. (1) of "Tail-Replay: Escaping the Curse of Linear Attention in
+ * Prefix Caching for Hybrid LLMs" (section 2) written on the transposed state
+ * (T_t = alpha_t (I - beta_t k_t k_t^T) is symmetric, so T_t S^T = (S T_t)^T).
+ * The readout is o_t = S_t (scale * q_t) with the updated state.
+ *
+ * Token-major inputs.  q, k: [total_tokens][h_k][d_k]; v and O: [total_tokens]
+ * [h_v][d_v]; g and beta: fp32 [total_tokens][h_v].  Sequences (replay tails)
+ * are packed back to back; cu_seqlens (int32, DEVICE memory, n_seqs + 1
+ * entries, non-decreasing, cu_seqlens[n_seqs] <= total_tokens) gives each
+ * one's token range.  v-head h reads q/k head h / (h_v / h_k) (consecutive
+ * v-heads share a key head).  States: fp32 [n_seqs][h_v][d_v][d_k].
+ *
+ * Ownership and memory.  Every pointer except the host arrays of gdn_compose
+ * is a DEVICE pointer owned by the caller; the library never frees or keeps
+ * them.  Calls that need scratch memory take it from a per-device pool that
+ * the library grows on first need with cudaMallocAsync on the caller's
+ * stream (stream-ordered) and keeps until process exit.
+ *
+ * Asynchrony and errors.  Every call only enqueues work on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and returns 0 (GDN_OK) or a
+ * negative GDN_ERR_* code without launching anything.  No exception crosses
+ * the ABI.  gdn_last_error() gives a thread-local message for the last
+ * failure.  Errors found on the device (malformed cu_seqlens) are recorded in
+ * a sticky per-device status word that gdn_get_status() returns and clears.
+ *
+ * Alignment.  q, k, v, O, S0, S_out, T and S_local base pointers must be
+ * 16-byte aligned; g, beta and cu_seqlens 4-byte aligned (else GDN_ERR_ALIGN).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* return codes */
+#define GDN_OK 0
+#define GDN_ERR_ARG (-1)         /* null pointer, negative size, bad flag */
+#define GDN_ERR_SHAPE (-2)       /* inconsistent sizes (h_v % h_k, token ranges) */
+#define GDN_ERR_ALIGN (-3)       /* a base pointer breaks the alignment rule */
+#define GDN_ERR_UNSUPPORTED (-4) /* a head size or dtype this build has no kernel for */
+#define GDN_ERR_CUDA (-5)        /* a CUDA runtime call failed (message in gdn_last_error) */
+#define GDN_ERR_TIMEOUT (-6)     /* a bounded device-side wait gave up */
+#define GDN_ERR_NOMEM (-7)       /* the scratch pool could not grow */
+
+/* storage type of q, k, v and O (g, beta and every state are always fp32) */
+#define GDN_F32 0
+#define GDN_BF16 1
+
+/* flags */
+#define GDN_QK_L2NORM 1u   /* normalise q and k per (token, head): x / sqrt(sum x^2 + 1e-6) */
+#define GDN_STATE_ONLY 2u  /* rebuild the state only; O_out may be NULL and is not written */
+#define GDN_PRECISE 4u     /* bf16 inputs: take the fp32 CUDA-core path instead of the tensor-core path */
+
+typedef struct {
+  int32_t n_seqs;       /* packed sequences (replay tails, or chunks for gdn_chunk_operator) */
+  int32_t total_tokens; /* rows of q, k, v, g, beta, O */
+  int32_t h_k;          /* q/k heads */
+  int32_t h_v;          /* v heads, a multiple of h_k */
+  int32_t d_k;          /* key/query head dim: a multiple of 8, at most 128 */
+  int32_t d_v;          /* value head dim: a multiple of 8, at most 128 */
+  int32_t dtype;        /* GDN_F32 or GDN_BF16 */
+  uint32_t flags;       /* GDN_QK_L2NORM | GDN_STATE_ONLY | GDN_PRECISE */
+  float scale;          /* multiplies q in the readout (1.0 when unsure) */
+} gdn_dims;
+
+/*
+ * gdn_replay -- rebuild each sequence's recurrent state by replaying its tail.
+ * Source: "Tail-Replay: ..." section 3, Eq. (2): the state at the start of
+ * the tail is S0 (zero when S0 == NULL, the method's zero-initialised
+ * replay), Eq. (1) is applied to every tail token, the final state is
+ * written to S_out and, unless GDN_STATE_ONLY, every token's readout to O_out.
+ *   q, k, v      inputs in `dims->dtype`, layouts above
+ *   g, beta      fp32 [total_tokens][h_v]; g = log(alpha) <= 0
+ *   cu_seqlens   int32 device [n_seqs + 1]
+ *   S0           fp32 [n_seqs][h_v][d_v][d_k] or NULL
+ *   O_out        [total_tokens][h_v][d_v] in `dims->dtype`; NULL iff GDN_STATE_ONLY.
+ *                Rows outside every sequence's range are not written.
+ *   S_out        fp32 [n_seqs][h_v][d_v][d_k]; may alias S0 (in-place update)
+ * Computation: chunks of 64 tokens, fp32 state carried between chunks.  bf16
+ * inputs run on the tcgen05 tensor cores; fp32 inputs (or GDN_PRECISE) on
+ * fp32 CUDA cores.
+ */
+int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
+               const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
+               void* stream);
+
+/*
+ * gdn_chunk_operator -- the affine operator of isolated chunks.
+ * Source: "LinearKV: One Cached State Suffices for Position-Independent
+ * Caching in Hybrid LLMs", composition passage: a chunk maps an entering
+ * state to T_C S_in + S_local (transposed-state form), T_C the product of its
+ * per-token transitions T_t = alpha_t (I - beta_t k_t k_t^T), latest on the
+ * left, and S_local the state it reaches from an empty start.
+ *   Each of the n_seqs ranges of cu_seqlens is one chunk (any length).  When
+ *   cu_seqlens == NULL, n_seqs must be 1 and the chunk is all total_tokens.
+ *   T_out       fp32 [n_seqs][h_v][d_k][d_k], T_C row-major, so that
+ *               S_out = S_in T_C^T + S_local in this ABI's state layout
+ *   Slocal_out  fp32 [n_seqs][h_v][d_v][d_k]
+ * q is not needed; dims->scale and GDN_STATE_ONLY are ignored.  Computed in
+ * fp32 on CUDA cores whatever the input dtype.
+ */
+int gdn_chunk_operator(const gdn_dims* dims, const void* k, const float* g, const float* beta, const void* v,
+                       const int32_t* cu_seqlens, float* T_out, float* Slocal_out, void* stream);
+
+/*
+ * gdn_compose -- apply K chunk operators back to back.
+ * Source: "LinearKV: ..." composition passage: the closed form
+ * S_K = T_{C_K}...T_{C_2} S_local_1 + ... + T_{C_K} S_local_{K-1} + S_local_K
+ * (transposed-state form), extended by T_{C_K}...T_{C_1} S_in when an
+ * entering state is given.  Evaluated as S <- S T_j^T + S_local_j, j = 1..K.
+ *   dims        uses h_v, d_k, d_v only (one state per v-head)
+ *   K           number of chunks, 0 <= K <= 256
+ *   T, Slocal   HOST arrays of K device pointers; T[j] fp32 [h_v][d_k][d_k],
+ *               Slocal[j] fp32 [h_v][d_v][d_k]
+ *   S_in        fp32 [h_v][d_v][d_k] or NULL (empty entering state)
+ *   S_out       fp32 [h_v][d_v][d_k]; must not alias any input
+ */
+int gdn_compose(const gdn_dims* dims, int32_t K, const float* const* T, const float* const* Slocal,
+                const float* S_in, float* S_out, void* stream);
+
+/*
+ * gdn_get_status -- synchronise `stream`, then return and clear the sticky
+ * device status of the current device: GDN_OK, GDN_ERR_SHAPE (a malformed
+ * cu_seqlens was skipped), GDN_ERR_TIMEOUT, or GDN_ERR_CUDA when the stream
+ * itself reports an error.
+ */
+int gdn_get_status(void* stream);
+
+/* Thread-local message of the last failed call ("" if none). */
+const char* gdn_last_error(void);
+
+/* Bytes of scratch the library's pool needs for this problem (0 if none). */
+size_t gdn_workspace_bytes(const gdn_dims* dims);
+
+/* GDN_ABI_VERSION of the loaded library. */
+int gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

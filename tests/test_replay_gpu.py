@@ -1,0 +1,159 @@
+"""GPU parity of gdn_replay / gdn_chunk_operator / gdn_compose against the fp64 oracle.
+
+Every call goes through the C ABI (libgdn.so via the thin binding); the
+oracle runs on the host on the same seeded inputs.  Errors are relative
+Frobenius norms over whole tensors.  Tolerances: 1e-5 for fp32 inputs,
+3e-3 for bf16 inputs (fp32 accumulation and state; O is rounded to bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_state_chunked_gb300 import _lib, api, synthetic
+from tests.gpu_util import TOL_BF16, TOL_F32, host, oracle_replay, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    _lib.load(build=True)
+    torch.cuda.init()
+
+
+def _run(x, **kw):
+    d = to_device(x)
+    O, S = api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["S0"], **kw)
+    torch.cuda.synchronize()
+    api.gdn_get_status()
+    return O, S
+
+
+def test_tiny_config_fp32():
+    """1 sequence, 2 heads, d_k = d_v = 64, 256-token tail, fp32, zero initial state."""
+    x = synthetic.workload_inputs("tiny")
+    O, S = _run(x)
+    S_ref, O_ref = oracle_replay(x)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+    assert rel_err(host(O), O_ref) <= TOL_F32
+
+
+RAGGED = [1, 63, 64, 65, 130, 0, 200]
+
+
+@pytest.mark.parametrize("d_k,d_v", [(64, 32), (128, 128), (16, 64), (128, 8)])
+@pytest.mark.parametrize("with_S0", [False, True])
+def test_ragged_batch_fp32(d_k, d_v, with_S0):
+    x = synthetic.make_replay_inputs(RAGGED, 2, 4, d_k, d_v, dtype="f32", seed=100 + d_k + d_v,
+                                     unit_qk=False, with_S0=with_S0)
+    O, S = _run(x, scale=0.5)
+    S_ref, O_ref = oracle_replay(x, scale=0.5)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+    assert rel_err(host(O), O_ref) <= TOL_F32
+
+
+def test_without_l2norm_fp32():
+    x = synthetic.make_replay_inputs([77, 129], 1, 2, 32, 32, dtype="f32", seed=7, with_S0=True)
+    O, S = _run(x, l2norm_qk=False)
+    S_ref, O_ref = oracle_replay(x, l2norm_qk=False)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+    assert rel_err(host(O), O_ref) <= TOL_F32
+
+
+def test_state_only_leaves_outputs_alone():
+    x = synthetic.make_replay_inputs([90, 3], 2, 2, 64, 64, dtype="f32", seed=8)
+    d = to_device(x)
+    _, S = api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], state_only=True)
+    torch.cuda.synchronize()
+    S_ref, _ = oracle_replay(x, want_O=False)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+
+
+def test_rows_outside_sequences_are_not_written():
+    x = synthetic.make_replay_inputs([50, 40], 1, 2, 32, 32, dtype="f32", seed=9)
+    d = to_device(x)
+    cu = torch.tensor([0, 50, 80], dtype=torch.int32, device="cuda")  # last 10 tokens belong to no sequence
+    O = torch.full((90, 2, 32), 7.0, device="cuda")
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, O_out=O)
+    torch.cuda.synchronize()
+    assert torch.all(O[80:] == 7.0)
+    S_ref, O_ref = oracle.replay(x.q, x.k, x.v, x.g, x.beta, [0, 50, 80])
+    assert rel_err(host(O[:80]), O_ref[:80]) <= TOL_F32
+
+
+def test_in_place_state_update():
+    x = synthetic.make_replay_inputs([70, 20], 1, 2, 32, 32, dtype="f32", seed=10, with_S0=True)
+    d = to_device(x)
+    S = d["S0"].clone()
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], S, S_out=S, state_only=True)
+    torch.cuda.synchronize()
+    S_ref, _ = oracle_replay(x, want_O=False)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+
+
+def test_malformed_cu_seqlens_sets_status_and_skips_sequence():
+    x = synthetic.make_replay_inputs([30, 30, 30], 1, 1, 16, 16, dtype="f32", seed=11)
+    d = to_device(x)
+    cu = torch.tensor([0, 30, 20, 90], dtype=torch.int32, device="cuda")  # sequence 1 runs backwards
+    S = torch.full((3, 1, 16, 16), 5.0, device="cuda")
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=True)
+    with pytest.raises(_lib.GdnError) as ei:
+        api.gdn_get_status()
+    assert ei.value.code == _lib.GDN_ERR_SHAPE
+    api.gdn_get_status()  # the status is cleared once read
+    assert torch.all(S[1] == 5.0)
+    S_ref, _ = oracle.replay(x.q, x.k, x.v, x.g, x.beta, [0, 30], want_O=False)
+    assert rel_err(host(S[0]), S_ref[0]) <= TOL_F32
+
+
+def test_precise_path_on_bf16_inputs():
+    x = synthetic.make_replay_inputs(RAGGED, 2, 4, 128, 128, dtype="bf16", seed=12, with_S0=True)
+    O, S = _run(x, precise=True)
+    S_ref, O_ref = oracle_replay(x)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+    assert rel_err(host(O), O_ref) <= TOL_BF16
+
+
+# ------------------------------------------------------------------ chunk operator and composition
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_operator_matches_oracle(dtype):
+    x = synthetic.make_replay_inputs([200, 1, 64, 129], 2, 4, 64, 32, dtype=dtype, seed=13, gate_scale=1e-3)
+    d = to_device(x)
+    T, Sl = api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], d["cu_seqlens"])
+    torch.cuda.synchronize()
+    T_ref, Sl_ref = oracle.chunk_operator(x.k, x.g, x.beta, x.v, x.cu_seqlens)
+    assert rel_err(host(T), T_ref) <= TOL_F32
+    assert rel_err(host(Sl), Sl_ref) <= TOL_F32
+
+
+def test_compose_matches_oracle_closed_form():
+    rng = np.random.Generator(np.random.PCG64(14))
+    K, h, dk, dv = 6, 4, 128, 128
+    T = (rng.standard_normal((K, h, dk, dk)) / np.sqrt(dk)).astype(np.float32)
+    Sl = rng.standard_normal((K, h, dv, dk)).astype(np.float32)
+    S_in = rng.standard_normal((h, dv, dk)).astype(np.float32)
+    Td = [torch.from_numpy(T[j]).cuda() for j in range(K)]
+    Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
+    out = api.gdn_compose(Td, Sd, torch.from_numpy(S_in).cuda())
+    out0 = api.gdn_compose(Td, Sd, None)
+    torch.cuda.synchronize()
+    assert rel_err(host(out), oracle.compose(T, Sl, S_in)) <= TOL_F32
+    assert rel_err(host(out0), oracle.compose(T, Sl, None)) <= TOL_F32
+
+
+def test_composed_chunks_equal_sequential_replay():
+    """LinearKV composition passage: composing isolated-chunk operators is exact, so
+    compose(chunk operators) on the GPU equals the GPU's own sequential replay."""
+    pieces = [300, 64, 1, 250]
+    x = synthetic.make_replay_inputs([sum(pieces)], 2, 4, 64, 64, dtype="f32", seed=15, gate_scale=1e-3)
+    d = to_device(x)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(pieces)]), dtype=torch.int32, device="cuda")
+    T, Sl = api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], cu)
+    SK = api.gdn_compose([T[j] for j in range(len(pieces))], [Sl[j] for j in range(len(pieces))])
+    _, S = api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], state_only=True)
+    torch.cuda.synchronize()
+    S_ref, _ = oracle_replay(x, want_O=False)
+    assert rel_err(host(SK), S_ref[0]) <= TOL_F32
+    assert rel_err(host(S[0]), S_ref[0]) <= TOL_F32
