@@ -99,7 +99,14 @@ int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v
   p.h_k = dims->h_k; p.h_v = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
   p.augmented = 0; p.l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
   p.write_O = state_only ? 0 : 1; p.scale = dims->scale; p.status = status;
-  cudaError_t e = launch_replay_simt(p, dims->dtype == GDN_BF16, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == GDN_BF16 && !(dims->flags & GDN_PRECISE)) {
+    int not_supported = 0;
+    cudaError_t e = launch_replay_tc(p, st, &not_supported);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_replay tensor-core launch");
+    if (!not_supported) return GDN_OK;
+  }
+  cudaError_t e = launch_replay_simt(p, dims->dtype == GDN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "gdn_replay launch");
   return GDN_OK;
 }

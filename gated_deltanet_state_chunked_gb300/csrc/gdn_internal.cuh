@@ -33,6 +33,11 @@ struct SimtParams {
 
 cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t stream);
 
+// Tensor-core path (bf16, d_k = d_v = 128).  Sets *not_supported (and launches
+// nothing) when the problem is outside what it handles.
+cudaError_t launch_replay_tc(const SimtParams& p, cudaStream_t stream, int* not_supported);
+int replay_tc_rows(int n_seqs, int h_v);
+
 constexpr int kMaxCompose = 256;  // largest K of one gdn_compose call
 
 // Passed by value: the K device pointers travel in the kernel parameters.
