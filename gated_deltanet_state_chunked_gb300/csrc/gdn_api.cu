@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstring>
 #include <cstdarg>
+#include <mutex>
 #include <string>
 
 #include "gdn_internal.cuh"
@@ -47,6 +48,31 @@ int check_token_dims(const gdn_dims* d) {
   return check_head_dims(d);
 }
 
+// Stream-ordered scratch: one private memory pool per device that keeps its memory
+// (release threshold = max), so after the first call allocations are pool hits.
+int scratch_pool(cudaMemPool_t* out) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    e = cudaMemPoolCreate(&pools[dev], &props);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = UINT64_MAX;
+    e = cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+  }
+  *out = pools[dev];
+  return GDN_OK;
+}
+
 }  // namespace
 
 int* device_status_word() {
@@ -66,8 +92,10 @@ int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 size_t gdn_workspace_bytes(const gdn_dims* dims) {
-  (void)dims;
-  return 0;
+  if (!dims || dims->dtype != GDN_BF16 || (dims->flags & GDN_PRECISE) || dims->d_k != kMaxHead ||
+      dims->d_v != kMaxHead || dims->total_tokens <= 0 || dims->n_seqs <= 0 || dims->h_v <= 0)
+    return 0;
+  return replay_tc_workspace_bytes(dims->n_seqs, dims->total_tokens, dims->h_v);
 }
 
 int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
@@ -100,11 +128,19 @@ int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v
   p.augmented = 0; p.l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
   p.write_O = state_only ? 0 : 1; p.scale = dims->scale; p.status = status;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dims->dtype == GDN_BF16 && !(dims->flags & GDN_PRECISE)) {
-    int not_supported = 0;
-    cudaError_t e = launch_replay_tc(p, st, &not_supported);
+  if (dims->dtype == GDN_BF16 && !(dims->flags & GDN_PRECISE) && replay_tc_supported(p)) {
+    const size_t bytes = replay_tc_workspace_bytes(p.n_seqs, p.total_tokens, p.h_v);
+    cudaMemPool_t pool = nullptr;
+    int prc = scratch_pool(&pool);
+    if (prc) return prc;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+    if (e != cudaSuccess) return fail(GDN_ERR_NOMEM, "scratch of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    e = launch_replay_tc(p, ws, bytes, st);
+    const cudaError_t ef = cudaFreeAsync(ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_replay tensor-core launch");
-    if (!not_supported) return GDN_OK;
+    if (ef != cudaSuccess) return cuda_fail(ef, "scratch release");
+    return GDN_OK;
   }
   cudaError_t e = launch_replay_simt(p, dims->dtype == GDN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "gdn_replay launch");

@@ -33,9 +33,12 @@ struct SimtParams {
 
 cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t stream);
 
-// Tensor-core path (bf16, d_k = d_v = 128).  Sets *not_supported (and launches
-// nothing) when the problem is outside what it handles.
-cudaError_t launch_replay_tc(const SimtParams& p, cudaStream_t stream, int* not_supported);
+// Tensor-core path (bf16 inputs, d_k = d_v = 128, total_tokens > 0): a chunk-parallel
+// prep kernel writes per-(chunk, v-head) records into `workspace`, then the scan
+// kernel walks each tail.  workspace_bytes must be >= replay_tc_workspace_bytes().
+bool replay_tc_supported(const SimtParams& p);
+size_t replay_tc_workspace_bytes(int n_seqs, int total_tokens, int h_v);
+cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 int replay_tc_rows(int n_seqs, int h_v);
 
 constexpr int kMaxCompose = 256;  // largest K of one gdn_compose call
