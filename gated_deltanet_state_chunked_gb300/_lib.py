@@ -58,6 +58,7 @@ _PD = ctypes.POINTER(GdnDims)
 
 SIGNATURES = {
     "gdn_replay": ([_PD, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "gdn_replay_noalloc": ([_PD, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "gdn_chunk_operator": ([_PD, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "gdn_compose": ([_PD, ctypes.c_int32, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "gdn_get_status": ([_VP], ctypes.c_int),

@@ -79,6 +79,45 @@ def gdn_replay(q, k, v, g, beta, cu_seqlens, S0=None, *, O_out=None, S_out=None,
     return O_out, S_out
 
 
+def gdn_replay_noalloc(q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, *, l2norm_qk=True, scale=1.0,
+                       state_only=False, precise=False, stream=None):
+    """gdn_replay for callers that cannot allocate device memory at call time.
+
+    Same arguments and results as gdn_replay, except that the outputs O_out
+    (None with ``state_only``) and S_out must be passed in: neither this
+    wrapper nor the library allocates anything.  The library's scratch is a
+    32 MiB static device array shared by all calls, so calls that overlap on
+    the GPU race; larger problems raise GdnError(GDN_ERR_NOMEM)."""
+    lib = _lib.load()
+    T, h_k, d_k = k.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    n = cu_seqlens.shape[0] - 1
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need_cuda("q", q, dt, (T, h_k, d_k))
+    _need_cuda("k", k, dt)
+    _need_cuda("v", v, dt, (T, h_v, d_v))
+    _need_cuda("g", g, torch.float32, (T, h_v))
+    _need_cuda("beta", beta, torch.float32, (T, h_v))
+    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    _need_cuda("S0", S0, torch.float32, (n, h_v, d_v, d_k))
+    if S_out is None or (O_out is None and not state_only):
+        raise ValueError("gdn_replay_noalloc needs caller-provided outputs")
+    _need_cuda("S_out", S_out, torch.float32, (n, h_v, d_v, d_k))
+    if not state_only:
+        _need_cuda("O_out", O_out, dt, (T, h_v, d_v))
+    else:
+        O_out = None
+    flags = (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_STATE_ONLY if state_only else 0) \
+        | (_lib.GDN_PRECISE if precise else 0)
+    dims = _lib.GdnDims(n, T, h_k, h_v, d_k, d_v, _DTYPE[dt], flags, float(scale))
+    rc = lib.gdn_replay_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                _ptr(cu_seqlens), _ptr(S0), _ptr(O_out), _ptr(S_out), _stream_handle(stream, k.device))
+    _lib.check(rc, "gdn_replay_noalloc")
+    return O_out, S_out
+
+
 def gdn_chunk_operator(k, g, beta, v, cu_seqlens=None, *, T_out=None, Slocal_out=None, l2norm_qk=True,
                        stream=None):
     """(T_C, S_local) of each chunk (range of cu_seqlens, or all tokens when None).

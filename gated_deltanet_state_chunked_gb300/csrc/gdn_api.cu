@@ -75,6 +75,45 @@ int scratch_pool(cudaMemPool_t* out) {
 
 }  // namespace
 
+// Argument checks of the allocation-free replay entry point (same rules as
+// gdn_replay): fills *p, sets *nothing_to_do for an empty batch.
+int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
+                      SimtParams* p, bool* nothing_to_do) {
+  g_last_error.clear();
+  *nothing_to_do = false;
+  if (!dims) return fail(GDN_ERR_ARG, "dims is NULL");
+  int rc = check_token_dims(dims);
+  if (rc) return rc;
+  const bool state_only = dims->flags & GDN_STATE_ONLY;
+  if (dims->n_seqs == 0) {
+    *nothing_to_do = true;
+    return GDN_OK;
+  }
+  if (!cu_seqlens || !S_out) return fail(GDN_ERR_ARG, "cu_seqlens and S_out are required");
+  if (!state_only && !O_out) return fail(GDN_ERR_ARG, "O_out is NULL without GDN_STATE_ONLY");
+  if (dims->total_tokens > 0 && (!q || !k || !v || !g || !beta))
+    return fail(GDN_ERR_ARG, "q, k, v, g and beta are required when total_tokens > 0");
+  const void* p16[] = {q, k, v, O_out, S0, S_out};
+  for (const void* ptr : p16)
+    if (ptr && !aligned(ptr, 16)) return fail(GDN_ERR_ALIGN, "q, k, v, O, S0 and S_out must be 16-byte aligned");
+  if (!aligned(g, 4) || !aligned(beta, 4) || !aligned(cu_seqlens, 4))
+    return fail(GDN_ERR_ALIGN, "g, beta and cu_seqlens must be 4-byte aligned");
+  int* status = device_status_word();
+  if (!status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
+  *p = SimtParams{};
+  p->q = q; p->k = k; p->v = v; p->g = g; p->beta = beta; p->cu = cu_seqlens; p->S0 = S0;
+  p->O = state_only ? nullptr : O_out;
+  p->S_out = S_out; p->T_out = nullptr;
+  p->n_seqs = dims->n_seqs; p->total_tokens = dims->total_tokens;
+  p->h_k = dims->h_k; p->h_v = dims->h_v; p->d_k = dims->d_k; p->d_v = dims->d_v;
+  p->augmented = 0; p->l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
+  p->write_O = state_only ? 0 : 1; p->scale = dims->scale; p->status = status;
+  return GDN_OK;
+}
+
+int report_error(int code, const char* message) { return fail(code, "%s", message); }
+
 int* device_status_word() {
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;

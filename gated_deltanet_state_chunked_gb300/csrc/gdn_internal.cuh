@@ -57,4 +57,10 @@ cudaError_t launch_compose_simt(const ComposeParams& p, cudaStream_t stream);
 // Sticky status word of the current device (device pointer).
 int* device_status_word();
 
+// Helpers of the allocation-free replay entry point (defined in gdn_api.cu).
+int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
+                      SimtParams* p, bool* nothing_to_do);
+int report_error(int code, const char* message);
+
 }  // namespace gdn

@@ -732,3 +732,65 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
 }
 
 }  // namespace gdn
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free replay: the same prep + scan kernels, with their scratch in a fixed static
+// device array instead of the stream-ordered pool.
+// ---------------------------------------------------------------------------------------------
+namespace gdn {
+namespace {
+
+// 32 MiB on every GPU that loads the library, held until process exit.  Enough for the
+// records of one 3277-token tail at 32 v-heads ((52 + 1) chunks x 32 heads x 17408 B).
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch, resolved once per device with that device current
+// (in host code the symbol itself is only a host-side stand-in).
+int static_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return report_error(GDN_ERR_CUDA, "cudaGetDevice failed");
+  if (dev < 0 || dev >= 64) return report_error(GDN_ERR_UNSUPPORTED, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess || !ptr) return report_error(GDN_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+    addr[dev] = ptr;
+  }
+  *out = addr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                                  const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out,
+                                  float* S_out, void* stream) {
+  using namespace gdn;
+  SimtParams p;
+  bool nothing = false;
+  int rc = check_replay_args(dims, q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, &p, &nothing);
+  if (rc || nothing) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == GDN_BF16 && !(dims->flags & GDN_PRECISE) && replay_tc_supported(p)) {
+    const size_t need = replay_tc_workspace_bytes(p.n_seqs, p.total_tokens, p.h_v);
+    if (need > kStaticScratchBytes)
+      return report_error(GDN_ERR_NOMEM,
+                          "gdn_replay_noalloc: the problem needs more scratch than the 32 MiB static array "
+                          "((ceil(total_tokens/64) + n_seqs) * h_v * 17408 bytes); use gdn_replay");
+    void* ws = nullptr;
+    rc = static_scratch_address(&ws);
+    if (rc) return rc;
+    const cudaError_t e = launch_replay_tc(p, ws, kStaticScratchBytes, st);
+    if (e != cudaSuccess) return report_error(GDN_ERR_CUDA, cudaGetErrorString(e));
+    return GDN_OK;
+  }
+  const cudaError_t e = launch_replay_simt(p, dims->dtype == GDN_BF16, st);  // needs no scratch
+  if (e != cudaSuccess) return report_error(GDN_ERR_CUDA, cudaGetErrorString(e));
+  return GDN_OK;
+}

@@ -100,6 +100,33 @@ int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v
                void* stream);
 
 /*
+ * gdn_replay_noalloc -- gdn_replay without any device allocation.
+ * The pages have no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory when they call it, for example a
+ * serving process that reserves almost all of the GPU's memory at start-up
+ * (for its cache) and forbids allocations afterwards, or a caller whose
+ * process-wide policy routes every device allocation through its own
+ * allocator.  gdn_replay takes its scratch from a pool that can grow; this
+ * variant instead uses one static device array of 32 MiB that every GPU that
+ * loads the library holds until the process exits.
+ *   Arguments, layouts, results and error codes are those of gdn_replay.
+ *   Limit: the tensor-core path needs (ceil(total_tokens / 64) + n_seqs) * h_v
+ *   * 17408 bytes of scratch (a 3277-token tail at 32 v-heads needs 29.5 MB);
+ *   a larger problem is rejected with GDN_ERR_NOMEM before anything is
+ *   launched.  fp32 inputs and GDN_PRECISE need no scratch.
+ *   The first call on a device resolves the static array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (on two
+ *   streams, or from two threads) race with each other and must be serialised
+ *   by the caller.  Every byte a call reads from the array is written by the
+ *   same call first, so nothing needs clearing between calls.
+ */
+int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                       const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
+                       void* stream);
+
+/*
  * gdn_chunk_operator -- the affine operator of isolated chunks.
  * Source: "LinearKV: One Cached State Suffices for Position-Independent
  * Caching in Hybrid LLMs", composition passage: a chunk maps an entering
