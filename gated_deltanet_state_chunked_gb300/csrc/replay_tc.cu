@@ -43,16 +43,27 @@ using namespace tcp;
 
 constexpr int NT = 256;
 
+// Named barrier over one 128-thread warpgroup (ids 1, 2; 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
 // ---------------------------------------------------------------------------------------------
 // prep kernel
 // ---------------------------------------------------------------------------------------------
 constexpr int MST = 68;  // row stride (floats) of the 64x64 fp32 work matrices
+// Inside one chunk the gate sums span fewer binades than this in all but extreme inputs; then
+// exp2(G_t - G_s) is evaluated as exp2(G_t - G_last) * exp2(G_last - G_s) without leaving the
+// fp32 range, else per element.
+constexpr float kFactorRange = 100.f;
+
 struct PrepLay {
-  static constexpr uint32_t KT = 0;                      // bf16 K tile: 2 d_k atoms x (64 rows x 128 B)
-  static constexpr uint32_t AMAT = 16384;                // fp32 64 x 68
-  static constexpr uint32_t MMAT = AMAT + 64 * MST * 4;  // fp32 64 x 68
-  static constexpr uint32_t GATE = MMAT + 64 * MST * 4;  // beta[64], G2[64], rk[64]
-  static constexpr uint32_t BARS = GATE + 768;           // 2 mbarriers, TMEM slot, scratch ints
+  static constexpr uint32_t KQ = 0;                      // bf16 [K;Q]: 2 d_k atoms x (128 rows x 128 B)
+  static constexpr uint32_t SLOT = 32768;                // two v-head slots:
+  static constexpr uint32_t AMAT = 0;                    //   fp32 64 x 68 (A, then block scratch)
+  static constexpr uint32_t MMAT = 64 * MST * 4;         //   fp32 64 x 68 (M)
+  static constexpr uint32_t GATE = 2 * 64 * MST * 4;     //   8 x 64 floats
+  static constexpr uint32_t SLOT_BYTES = GATE + 2048;
+  static constexpr uint32_t COMMON = SLOT + 2 * SLOT_BYTES;  // rk[64], rq[64]
+  static constexpr uint32_t BARS = COMMON + 512;
   static constexpr uint32_t TOTAL = BARS + 128;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
@@ -63,38 +74,39 @@ struct PrepParams {
   const int32_t* cu;
   unsigned char* rec;  // records [chunk][h_v]
   int* status;
-  int n_seqs, total_tokens, h_k, h_v, l2norm;
+  int n_seqs, total_tokens, h_k, h_v, l2norm, write_O;
+  float scale;
 };
 
-// M = (I + A)^{-1} for a 64x64 strictly lower A (stride MST).  256 threads.
-// A's strictly upper blocks are used as scratch (overwritten).
-__device__ void invert_unit_lower(float* A, float* M) {
-  const int tid = threadIdx.x;
-  if (tid < 64) {  // diagonal blocks by forward substitution, one column per thread
-    const int b = tid >> 4, j = tid & 15;
+// M = (I + A)^{-1} for a 64x64 strictly lower A (stride MST), by one 128-thread warpgroup
+// (t = thread index in the group, bid = its named barrier).  A's strictly upper blocks are
+// used as scratch.  Diagonal 16x16 blocks by substitution; then At_ik = M_ii A_ik and
+// M_ij = -sum_{k=j}^{i-1} At_ik M_kj along the block diagonals.
+__device__ void invert_unit_lower(float* A, float* M, int t, int bid) {
+  if (t < 64) {
+    const int b = t >> 4, j = t & 15;
     const float* Ab = A + (16 * b) * MST + 16 * b;
     float m[16];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float a0 = (t == j) ? 1.f : 0.f, a1 = 0.f;
+    for (int r = 0; r < 16; ++r) {
+      float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-      for (int s = 0; s < t; s += 2) {
-        a0 = fmaf(-Ab[t * MST + s], m[s], a0);
-        if (s + 1 < t) a1 = fmaf(-Ab[t * MST + s + 1], m[s + 1], a1);
+      for (int s = 0; s < r; s += 2) {
+        a0 = fmaf(-Ab[r * MST + s], m[s], a0);
+        if (s + 1 < r) a1 = fmaf(-Ab[r * MST + s + 1], m[s + 1], a1);
       }
-      m[t] = a0 + a1;
+      m[r] = a0 + a1;
     }
 #pragma unroll
-    for (int t = 0; t < 16; ++t) M[(16 * b + t) * MST + 16 * b + j] = m[t];
+    for (int r = 0; r < 16; ++r) M[(16 * b + r) * MST + 16 * b + j] = m[r];
   } else {
-    for (int i = tid - 64; i < 64 * 64; i += NT - 64) {
-      const int t = i >> 6, s = i & 63;
-      if ((s >> 4) > (t >> 4)) M[t * MST + s] = 0.f;
+    for (int i = t - 64; i < 64 * 16; i += 64) {  // zero the strictly upper blocks, 4 at a time
+      const int r = i >> 4, c4 = (i & 15) * 4;
+      if ((c4 >> 4) > (r >> 4)) *reinterpret_cast<float4*>(M + r * MST + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  __syncthreads();
-  // At_ik = M_ii A_ik for the six strictly lower blocks, kept in A's block (k, i)
-  for (int task = tid; task < 384; task += NT) {
+  group_sync(bid);
+  for (int task = t; task < 384; task += 128) {
     const int blk = task >> 6, r = (task >> 2) & 15, cq = (task & 3) * 4;
     const int i = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
     const int k = blk < 1 ? 0 : (blk < 3 ? blk - 1 : blk - 3);
@@ -108,11 +120,10 @@ __device__ void invert_unit_lower(float* A, float* M) {
     }
     *reinterpret_cast<float4*>(A + (16 * k + r) * MST + 16 * i + cq) = acc;
   }
-  __syncthreads();
-  // M_ij = -sum_{k=j}^{i-1} At_ik M_kj, block diagonals d = 1, 2, 3
+  group_sync(bid);
 #pragma unroll
   for (int d = 1; d < 4; ++d) {
-    for (int task = tid; task < (4 - d) * 64; task += NT) {
+    for (int task = t; task < (4 - d) * 64; task += 128) {
       const int i = d + (task >> 6), j = i - d, r = (task >> 2) & 15, cq = (task & 3) * 4;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int k = j; k < i; ++k) {
@@ -126,22 +137,37 @@ __device__ void invert_unit_lower(float* A, float* M) {
       }
       *reinterpret_cast<float4*>(M + (16 * i + r) * MST + 16 * j + cq) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
-    __syncthreads();
+    group_sync(bid);
   }
 }
 
-__global__ void __launch_bounds__(NT, 4) chunk_prep_kernel(const __grid_constant__ CUtensorMap map_k, PrepParams p) {
+// Row sum of squares of a 64-element bf16 row held as 8 16-byte chunks (any order).
+__device__ __forceinline__ float row_sumsq(const unsigned char* row, int rot) {
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 u = reinterpret_cast<const uint4*>(row)[(c + rot) & 7];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
+  }
+  return ss;
+}
+
+__global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant__ CUtensorMap map_q,
+                                                           const __grid_constant__ CUtensorMap map_k, PrepParams p) {
   using L = PrepLay;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  float* amat = reinterpret_cast<float*>(sm + L::AMAT);
-  float* mmat = reinterpret_cast<float*>(sm + L::MMAT);
-  float* gBeta = reinterpret_cast<float*>(sm + L::GATE);
-  float* gG2 = gBeta + 64;
-  float* gRk = gBeta + 128;
+  float* cRk = reinterpret_cast<float*>(sm + L::COMMON);
+  float* cRq = cRk + 64;
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + L::BARS);
   uint64_t* bar_mma = bar_tma + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 16);
+  int* fact = reinterpret_cast<int*>(sm + L::BARS + 24);  // [2], per slot
   int* scratch = reinterpret_cast<int*>(sm + L::BARS + 32);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = warp >> 2;
@@ -160,9 +186,11 @@ __global__ void __launch_bounds__(NT, 4) chunk_prep_kernel(const __grid_constant
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
     mbar_fence_init();
-    mbar_arrive_expect_tx(bar_tma, 16384);
-    tma_load_2d(sm + L::KT, &map_k, bar_tma, hk * DK, t0);
-    tma_load_2d(sm + L::KT + 8192, &map_k, bar_tma, hk * DK + 64, t0);
+    mbar_arrive_expect_tx(bar_tma, 32768);
+    for (int a = 0; a < 2; ++a) {
+      tma_load_2d(sm + L::KQ + a * 16384, &map_k, bar_tma, hk * DK + a * 64, t0);
+      tma_load_2d(sm + L::KQ + a * 16384 + 8192, &map_q, bar_tma, hk * DK + a * 64, t0);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -170,47 +198,53 @@ __global__ void __launch_bounds__(NT, 4) chunk_prep_kernel(const __grid_constant
   const uint32_t tmem = *tmem_slot;
   bool ok = mbar_wait(bar_tma, 0, kWaitNs);
   if (tid == 0) {
-    const uint32_t k0 = smem_u32(sm + L::KT);
-    constexpr uint32_t id = idesc_bf16(64, 64, false, false);
+    const uint64_t d = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);
+    constexpr uint32_t id = idesc_bf16(128, 64, false, false);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const uint64_t d = sdesc_sw128(k0 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024);
-      mma_bf16(tmem, d, d, id, j > 0);
+      const uint64_t dj = d + (uint64_t)((((j >> 2) * 16384) + (j & 3) * 32) >> 4);
+      mma_bf16(tmem, dj, dj, id, j > 0);
     }
     mma_commit(bar_mma);
   }
-  if (tid < 128) {  // key norms from the bf16 tile (row sums need no un-swizzling)
+  {  // norms: 128 rows (64 keys, 64 queries) x 2 atoms, rotated chunk order (no bank conflicts)
     const int row = tid >> 1, atom = tid & 1;
-    const uint4* src = reinterpret_cast<const uint4*>(sm + L::KT + atom * 8192 + row * 128);
-    float ss = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 u = src[c];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-        ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-      }
-    }
+    float ss = row_sumsq(sm + L::KQ + atom * 16384 + row * 128, row);
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    if (atom == 0) gRk[row] = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
+    if (atom == 0) {
+      const float r = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
+      if (row < 64) cRk[row] = r;
+      else cRq[row - 64] = r * p.scale;
+    }
   }
   ok = mbar_wait(bar_mma, 0, kWaitNs) && ok;
   tc_fence_after();
-  float kk[32];  // this thread's 32 columns of K K^T (M=64 layout: rows 16*quad + lane, lane < 16)
-  tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + half * 32, kk);
+  float kq[32];  // row (32*quad + lane) of [K;Q] K^T, columns [32*half, +32)
+  tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + half * 32, kq);
   tmem_ld_wait();
   if (!ok && tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
+  __syncthreads();
 
-  for (int j = 0; j < G; ++j) {
-    const int h = hk * G + j;
-    __syncthreads();
-    if (warp == 0) {  // gates: beta, inclusive gate sums (log2 units); padding gets 0
+  const int slot = half, gt = tid & 127;  // warpgroup = v-head slot
+  unsigned char* sslot = sm + L::SLOT + slot * L::SLOT_BYTES;
+  float* amat = reinterpret_cast<float*>(sslot + L::AMAT);
+  float* mmat = reinterpret_cast<float*>(sslot + L::MMAT);
+  float* gB = reinterpret_cast<float*>(sslot + L::GATE);  // beta
+  float* gG2 = gB + 64;   // G log2(e)
+  float* gFa = gB + 128;  // beta_t rk_t exp2(G_t - G_last)
+  float* gFc = gB + 192;  // rk_s exp2(G_last - G_s)
+  float* gPa = gB + 256;  // rq_t exp2(G_t - G_last)
+  float* gGam = gB + 320; // gamma_t
+
+  for (int pair = 0; pair < G; pair += 2) {
+    const int nslots = min(2, G - pair);
+    // gates of both slots: warp 0 of each warpgroup
+    if ((warp & 3) == 0 && slot < nslots) {
+      const int h = hk * G + pair + slot;
       float ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
       float gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
-      gBeta[lane] = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-      gBeta[lane + 32] = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+      const float ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+      const float bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float xa = __shfl_up_sync(0xffffffffu, ga, o);
@@ -218,32 +252,100 @@ __global__ void __launch_bounds__(NT, 4) chunk_prep_kernel(const __grid_constant
         if (lane >= o) { ga += xa; gb += xb; }
       }
       gb += __shfl_sync(0xffffffffu, ga, 31);
-      gG2[lane] = ga * kLog2e;
-      gG2[lane + 32] = gb * kLog2e;
+      const float la = ga * kLog2e, lb = gb * kLog2e, last = __shfl_sync(0xffffffffu, lb, 31);
+      const float ea = exp2f(la - last), eb = exp2f(lb - last), fa = exp2f(last - la), fb = exp2f(last - lb);
+      gB[lane] = ba; gB[lane + 32] = bb;
+      gG2[lane] = la; gG2[lane + 32] = lb;
+      gFa[lane] = ba * cRk[lane] * ea; gFa[lane + 32] = bb * cRk[lane + 32] * eb;
+      gFc[lane] = cRk[lane] * fa; gFc[lane + 32] = cRk[lane + 32] * fb;
+      gPa[lane] = cRq[lane] * ea; gPa[lane + 32] = cRq[lane + 32] * eb;
+      gGam[lane] = exp2f(la); gGam[lane + 32] = exp2f(lb);
+      if (lane == 0) fact[slot] = (la - last) < kFactorRange ? 1 : 0;
     }
     __syncthreads();
-    if (lane < 16) {
-      const int t = 16 * quad + lane;
-      const float bt = gBeta[t] * gRk[t], gt = gG2[t];
+    // A (key rows) and P (query rows) for each slot from this thread's Gram row
+    {
+      const int row = 32 * quad + lane;
+      for (int sl = 0; sl < nslots; ++sl) {
+        unsigned char* ss_ = sm + L::SLOT + sl * L::SLOT_BYTES;
+        float* A_ = reinterpret_cast<float*>(ss_ + L::AMAT);
+        const float* B_ = reinterpret_cast<const float*>(ss_ + L::GATE);
+        const float *G2_ = B_ + 64, *Fa_ = B_ + 128, *Fc_ = B_ + 192, *Pa_ = B_ + 256;
+        if (row < 64) {
+          const int t = row;
+          if (fact[sl]) {
+            const float at = Fa_[t];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int s = half * 32 + i;
-        amat[t * MST + s] = s < t ? bt * exp2f(gt - gG2[s]) * gRk[s] * kk[i] : 0.f;
+            for (int i = 0; i < 32; ++i) {
+              const int s = half * 32 + i;
+              A_[t * MST + s] = s < t ? at * Fc_[s] * kq[i] : 0.f;
+            }
+          } else {
+            const float bt = B_[t] * cRk[t], g_t = G2_[t];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int s = half * 32 + i;
+              A_[t * MST + s] = s < t ? bt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i] : 0.f;
+            }
+          }
+        } else if (p.write_O) {
+          const int t = row - 64;
+          const int h = hk * G + pair + sl;
+          unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP;
+          float x[32];
+          if (fact[sl]) {
+            const float at = Pa_[t];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int s = half * 32 + i;
+              x[i] = s <= t ? tf32r(at * Fc_[s] * kq[i]) : 0.f;
+            }
+          } else {
+            const float qt = cRq[t], g_t = G2_[t];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int s = half * 32 + i;
+              x[i] = s <= t ? tf32r(qt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i]) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(rec + kf32(t, half * 32 + i, 64)) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+        }
       }
     }
     __syncthreads();
-    invert_unit_lower(amat, mmat);
-    // record
-    unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes;
-    for (int i = tid; i < 64 * 16; i += NT) {
-      const int t = i >> 4, q4 = (i & 15) * 4;
-      *reinterpret_cast<float4*>(rec + kRecM + (t * 64 + q4) * 4) = *reinterpret_cast<const float4*>(mmat + t * MST + q4);
+    if (slot < nslots) {
+      invert_unit_lower(amat, mmat, gt, 1 + slot);
+      // record: Mb hi|lo, Mw, per-token factors
+      const int h = hk * G + pair + slot;
+      unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes;
+      const int t = gt >> 1, s0 = (gt & 1) * 32;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        __align__(16) __nv_bfloat16 bh[8], bl[8], wv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int s = s0 + 8 * c + e;
+          const float m = mmat[t * MST + s];
+          const float mb = m * gB[s];
+          bh[e] = __float2bfloat16_rn(mb);
+          bl[e] = __float2bfloat16_rn(mb - __bfloat162float(bh[e]));
+          wv[e] = __float2bfloat16_rn(mb * gGam[s] * cRk[s]);
+        }
+        const int s = s0 + 8 * c;
+        *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(bh);
+        *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, 64 + s, 64)) = *reinterpret_cast<const uint4*>(bl);
+        *reinterpret_cast<uint4*>(rec + kRecMW + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(wv);
+      }
+      if (gt < 64) {
+        float* gate = reinterpret_cast<float*>(rec + kRecGate);
+        gate[gt] = gGam[gt];
+        gate[64 + gt] = gFc[gt];
+        gate[128 + gt] = gGam[gt] * cRq[gt];
+      }
     }
-    if (tid < 64) {
-      reinterpret_cast<float*>(rec + kRecBeta)[tid] = gBeta[tid];
-      reinterpret_cast<float*>(rec + kRecG2)[tid] = gG2[tid];
-      reinterpret_cast<float*>(rec + kRecRk)[tid] = gRk[tid];
-    }
+    __syncthreads();
   }
   tc_fence_before();
   __syncthreads();
@@ -255,28 +357,26 @@ __global__ void __launch_bounds__(NT, 4) chunk_prep_kernel(const __grid_constant
 // ---------------------------------------------------------------------------------------------
 template <int R>
 struct ScanLay {
-  static constexpr uint32_t KQ = 0;                 // bf16 [K;Q]: 2 d_k atoms x (128 rows x 128 B)
-  static constexpr uint32_t VT = KQ + 32768;        // bf16 V atom: 64 tokens x 128 B
-  static constexpr uint32_t REC = VT + 8192;        // the chunk's record (M, beta, G2, rk)
-  static constexpr uint32_t XR = REC + kRecBytes;   // 32 KB, three lives per chunk:
-  static constexpr uint32_t MB = XR;                //   bf16 [Mb_hi|Mb_lo] (64 rows x 2 atoms)
-  static constexpr uint32_t MW = XR + 16384;        //   bf16 [Mw_hi|Mw_lo]
-  static constexpr uint32_t WQ = XR;                //   fp32 W (64 rows x 4 atoms), tf32-rounded
-  static constexpr uint32_t UH = XR;                //   bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
-  static constexpr uint32_t UT = XR + 16384;        //   fp32 U^T (R rows x 2 atoms)
-  static constexpr uint32_t S32 = XR + 32768;       // fp32 state slice (R rows x 4 atoms), tf32-rounded
+  static constexpr uint32_t KQ = 0;                 // 2 buffers of bf16 [K;Q]: 2 d_k atoms x (128 rows x 128 B)
+  static constexpr uint32_t VT = KQ + 65536;        // bf16 V atom: 64 tokens x 128 B
+  static constexpr uint32_t R1 = VT + 8192;         // record part 1: Mb hi|lo (16 KB), Mw (8 KB)
+  static constexpr uint32_t R2 = R1 + kRecPart1;    // 2 buffers of record part 2: P (16 KB), factors (1 KB)
+  static constexpr uint32_t WQ = R2 + 2 * 18432;    // fp32 W (64 rows x 4 atoms), tf32-rounded
+  static constexpr uint32_t UH = WQ + 32768;        // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
+  static constexpr uint32_t UT = UH + 16384;        // fp32 U^T (R rows x 2 atoms)
+  static constexpr uint32_t S32 = UT + R * 256;     // fp32 state slice (R rows x 4 atoms), tf32-rounded
   static constexpr uint32_t SHL = S32 + R * 512;    // bf16 state hi (R rows x 2 atoms), then lo
-  static constexpr uint32_t P32 = SHL + R * 512;    // fp32 P (64 rows x 2 atoms)
-  static constexpr uint32_t GATE = P32 + 16384;     // gamma[64], wsc[64], rq[64], G2-scratch
-  static constexpr uint32_t BARS = GATE + 1024;
+  static constexpr uint32_t BARS = SHL + R * 512;
   static constexpr uint32_t TOTAL = BARS + 128;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
   // TMEM columns
-  static constexpr uint32_t cQK = 0, cW = 64, cU = 192, cD1w = 192 + R, cD1q = 192 + 2 * R, cD2 = 192 + 3 * R,
-                            cPU = 192 + 4 * R;
-  static_assert(192 + 5 * R <= 512, "TMEM columns");
+  static constexpr uint32_t cW = 0, cU = 128, cD1w = 128 + R, cD1q = 128 + 2 * R, cD2 = 128 + 3 * R,
+                            cPU = 128 + 4 * R;
+  static constexpr uint32_t TMEM_COLS = (128 + 5 * R) <= 256 ? 256 : 512;
+  static_assert(128 + 5 * R <= 512, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
-  static_assert(XR % 1024 == 0 && S32 % 1024 == 0 && P32 % 1024 == 0, "tile alignment");
+  static_assert(R2 % 1024 == 0 && WQ % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 && S32 % 1024 == 0,
+                "tile alignment");
 };
 
 struct ScanParams {
@@ -287,8 +387,7 @@ struct ScanParams {
   float* S_out;
   int* status;
   int n_seqs, total_tokens, h_k, h_v;
-  int l2norm, write_O;
-  float scale;
+  int write_O;
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -301,6 +400,9 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
 __device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
 
+// Advance a shared-memory descriptor's start address by a byte offset (multiple of 16).
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 template <int R>
 __global__ void __launch_bounds__(NT, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -309,18 +411,13 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr int HALF = R / 2;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const float* rM = reinterpret_cast<const float*>(sm + L::REC + kRecM);
-  const float* rBeta = reinterpret_cast<const float*>(sm + L::REC + kRecBeta);
-  const float* rG2 = reinterpret_cast<const float*>(sm + L::REC + kRecG2);
-  const float* rRk = reinterpret_cast<const float*>(sm + L::REC + kRecRk);
-  float* gGam = reinterpret_cast<float*>(sm + L::GATE);
-  float* gWsc = gGam + 64;
-  float* gRq = gGam + 128;
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + L::BARS);
-  uint64_t* bar_qk = bar_tma + 1;
-  uint64_t* bar_mma = bar_tma + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 24);
-  int* abort_flag = reinterpret_cast<int*>(sm + L::BARS + 28);
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + L::BARS);  // [2]: [K;Q] buffers
+  uint64_t* bar_r2 = bar_kq + 2;                                  // [2]: record part 2 buffers
+  uint64_t* bar_r1 = bar_kq + 4;                                  // V + record part 1
+  uint64_t* bar_a = bar_kq + 5;
+  uint64_t* bar_b = bar_kq + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 56);
+  int* flags = reinterpret_cast<int*>(sm + L::BARS + 60);
   int* scratch = reinterpret_cast<int*>(sm + L::BARS + 64);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -328,6 +425,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int slice = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int row0 = slice * R;
   const int hk = h / (p.h_v / p.h_k);
+  const bool issA = tid == 0, issB = tid == 128;  // the two MMA-issuing threads
 
   const int t_begin = p.cu[seq], t_end = p.cu[seq + 1];
   if (t_begin < 0 || t_end < t_begin || t_end > p.total_tokens) {
@@ -337,18 +435,35 @@ __global__ void __launch_bounds__(NT, 1)
   const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
 
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
+  auto rec_of = [&](int gc) { return p.rec + ((size_t)gc * p.h_v + h) * kRecBytes; };
+  auto load_kq_r2 = [&](int t0c, int gc, int b) {  // thread 0 only
+    mbar_arrive_expect_tx(&bar_kq[b], 32768);
+    for (int a = 0; a < 2; ++a) {
+      tma_load_2d(sm + L::KQ + b * 32768 + a * 16384, &map_k, &bar_kq[b], hk * DK + a * 64, t0c);
+      tma_load_2d(sm + L::KQ + b * 32768 + a * 16384 + 8192, &map_q, &bar_kq[b], hk * DK + a * 64, t0c);
+    }
+    mbar_arrive_expect_tx(&bar_r2[b], kRecPart2);
+    bulk_load(sm + L::R2 + b * 18432, rec_of(gc) + kRecPart1, kRecPart2, &bar_r2[b]);
+  };
+  auto load_v_r1 = [&](int t0c, int gc) {  // thread 0 only
+    mbar_arrive_expect_tx(bar_r1, 8192 + kRecPart1);
+    tma_load_2d(sm + L::VT, &map_v, bar_r1, h * DV + (row0 & ~63), t0c);
+    bulk_load(sm + L::R1, rec_of(gc), kRecPart1, bar_r1);
+  };
   if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_qk, 1);
-    mbar_init(bar_mma, 1);
+    for (int i = 0; i < 7; ++i) mbar_init(&bar_kq[i], 1);
     mbar_fence_init();
-    *abort_flag = 0;
+    flags[0] = 0;
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
+    if (t_begin < t_end) {
+      load_kq_r2(t_begin, ci.first, 0);
+      load_v_r1(t_begin, ci.first);
+    }
   }
 
   // entering state: thread owns d = 32*quad + lane and columns [half*HALF, +HALF), fp32 registers
@@ -372,130 +487,61 @@ __global__ void __launch_bounds__(NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-  const uint32_t sKQ = smem_u32(sm + L::KQ), sVT = smem_u32(sm + L::VT), sXR = smem_u32(sm + L::XR);
-  const uint32_t sS32 = smem_u32(sm + L::S32), sSHL = smem_u32(sm + L::SHL), sP32 = smem_u32(sm + L::P32);
   const uint32_t vcoloff = (uint32_t)(row0 & 63) * 2u;
-  uint32_t tma_ph = 0, qk_ph = 0, mma_ph = 0;
+  // base descriptors (start address advanced per K step with dadd)
+  const uint64_t dKQk = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);      // K-major view of [K;Q]
+  const uint64_t dKQmn = sdesc_sw128(smem_u32(sm + L::KQ), 16384, 1024);  // MN-major view of K
+  const uint64_t dVT = sdesc_sw128(smem_u32(sm + L::VT) + vcoloff, 8192, 1024);
+  const uint64_t dR1 = sdesc_sw128(smem_u32(sm + L::R1), 16, 1024);
+  const uint64_t dR2 = sdesc_sw128(smem_u32(sm + L::R2), 16, 1024);
+  const uint64_t dWQ = sdesc_sw128(smem_u32(sm + L::WQ), 16, 1024);
+  const uint64_t dUHmn = sdesc_sw128(smem_u32(sm + L::UH), 16384, 1024);
+  const uint64_t dUT = sdesc_sw128(smem_u32(sm + L::UT), 16, 1024);
+  const uint64_t dS32 = sdesc_sw128(smem_u32(sm + L::S32), 16, 1024);
+  const uint64_t dSHL = sdesc_sw128(smem_u32(sm + L::SHL), 16, 1024);
+  uint32_t kq_ph[2] = {0, 0}, r2_ph[2] = {0, 0}, r1_ph = 0, a_ph = 0, b_ph = 0;
   bool ok = true;
+  auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
+    if (!mbar_wait(bar, ph & 1, kWaitNs)) flags[0] = 1;
+    ++ph;
+  };
   int gcur = ci.first;
+  int buf = 0;
 
-  for (int t0 = t_begin; t0 < t_end; t0 += C, ++gcur) {
+  for (int t0 = t_begin; t0 < t_end; t0 += C, ++gcur, buf ^= 1) {
     const int n = min(C, t_end - t0);
-    // ---------------------------------------------------------------- loads
-    if (tid == 0) {
-      fence_async_smem();
-      mbar_arrive_expect_tx(bar_tma, 32768 + 8192 + kRecBytes);
-      for (int a = 0; a < 2; ++a) {
-        tma_load_2d(sm + L::KQ + a * 16384, &map_k, bar_tma, hk * DK + a * 64, t0);
-        tma_load_2d(sm + L::KQ + a * 16384 + 8192, &map_q, bar_tma, hk * DK + a * 64, t0);
-      }
-      tma_load_2d(sm + L::VT, &map_v, bar_tma, h * DV + (row0 & ~63), t0);
-      bulk_load(sm + L::REC, p.rec + ((size_t)gcur * p.h_v + h) * kRecBytes, kRecBytes, bar_tma);
-    }
-    if (!mbar_wait(bar_tma, tma_ph & 1, kWaitNs)) *abort_flag = 1;
-    ++tma_ph;
+    const uint32_t kqo = (uint32_t)buf * 32768u, r2o = (uint32_t)buf * 18432u;
+    const float* gate = reinterpret_cast<const float*>(sm + L::R2 + r2o + (kRecGate - kRecPart1));
+    wait_bar(&bar_kq[buf], kq_ph[buf]);
+    wait_bar(bar_r1, r1_ph);
     __syncthreads();
-    if (*abort_flag) { ok = false; break; }
-    // ---------------------------------------------------------------- Q K^T (outputs only)
-    if (tid == 0 && p.write_O) {
-      tc_fence_after();
-      constexpr uint32_t id = idesc_bf16(64, 64, false, false);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t off = (j >> 2) * 16384 + (j & 3) * 32;
-        mma_bf16(tmem + L::cQK, sdesc_sw128(sKQ + 8192 + off, 16, 1024), sdesc_sw128(sKQ + off, 16, 1024), id, j > 0);
-      }
-      mma_commit(bar_qk);
-    }
-    // gates, query norms, and the bf16 hi|lo factors Mb = M diag(beta), Mw = M diag(beta gamma rk)
-    if (tid < 64) {
-      const float l = rG2[63];
-      gGam[tid] = exp2f(rG2[tid]);
-      gWsc[tid] = exp2f(l - rG2[tid]) * rRk[tid];
-    } else if (tid < 192 && p.write_O) {
-      const int row = (tid - 64) >> 1, atom = tid & 1;
-      const uint4* src = reinterpret_cast<const uint4*>(sm + L::KQ + atom * 16384 + 8192 + row * 128);
-      float ss = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 u = src[c];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-        }
-      }
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (atom == 0) gRq[row] = (p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f) * p.scale;
-    }
-    {
-      const int t = tid >> 2, s0 = (tid & 3) * 16;
-      __align__(16) __nv_bfloat16 bh[16], bl[16], wh[16], wl[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int s = s0 + i;
-        const float mb = rM[t * 64 + s] * rBeta[s];
-        const float mw = mb * exp2f(rG2[s]) * rRk[s];
-        bh[i] = __float2bfloat16_rn(mb);
-        bl[i] = __float2bfloat16_rn(mb - __bfloat162float(bh[i]));
-        wh[i] = __float2bfloat16_rn(mw);
-        wl[i] = __float2bfloat16_rn(mw - __bfloat162float(wh[i]));
-      }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int s = s0 + 8 * c;
-        *reinterpret_cast<uint4*>(sm + L::MB + kbf16(t, s, 64)) = reinterpret_cast<const uint4*>(bh)[c];
-        *reinterpret_cast<uint4*>(sm + L::MB + kbf16(t, 64 + s, 64)) = reinterpret_cast<const uint4*>(bl)[c];
-        *reinterpret_cast<uint4*>(sm + L::MW + kbf16(t, s, 64)) = reinterpret_cast<const uint4*>(wh)[c];
-        *reinterpret_cast<uint4*>(sm + L::MW + kbf16(t, 64 + s, 64)) = reinterpret_cast<const uint4*>(wl)[c];
-      }
-    }
-    fence_async_smem();
-    __syncthreads();
-    // ---------------------------------------------------------------- W = Mw K, U~ = Mb V
-    if (tid == 0) {
+    if (flags[0]) { ok = false; break; }
+    // ---------------------------------------------------------------- W = Mw K (A), U~ = Mb V (B)
+    if (issA) {
       tc_fence_after();
       constexpr uint32_t idW = idesc_bf16(64, 128, false, true);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        mma_bf16(tmem + L::cW, dadd(dR1, kRecMW + j * 32), dadd(dKQmn, kqo + j * 2048), idW, j > 0);
+      mma_commit(bar_a);
+    } else if (issB) {
+      tc_fence_after();
       constexpr uint32_t idU = idesc_bf16(64, R, false, true);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t kb = (j >> 2) * 8192 + (j & 3) * 32;
-        const uint32_t rows = (j & 3) * 16 * 128;
-        mma_bf16(tmem + L::cW, sdesc_sw128(sXR + 16384 + kb, 16, 1024), sdesc_sw128(sKQ + rows, 16384, 1024), idW,
+      for (int j = 0; j < 8; ++j)
+        mma_bf16(tmem + L::cU, dadd(dR1, kRecMB + (j >> 2) * 8192 + (j & 3) * 32), dadd(dVT, (j & 3) * 2048), idU,
                  j > 0);
-        mma_bf16(tmem + L::cU, sdesc_sw128(sXR + kb, 16, 1024), sdesc_sw128(sVT + vcoloff + rows, 8192, 1024), idU,
-                 j > 0);
-      }
-      mma_commit(bar_mma);
+      mma_commit(bar_b);
     }
-    __syncwarp();
-    // ---------------------------------------------------------------- P (outputs only)
-    if (p.write_O) {
-      if (!mbar_wait(bar_qk, qk_ph & 1, kWaitNs)) *abort_flag = 1;
-      ++qk_ph;
-      tc_fence_after();
-      float v[32];
-      ld_cols(tmem + lane_base + L::cQK + half * 32, v);
-      tmem_ld_wait();
-      if (lane < 16) {
-        const int t = 16 * quad + lane;
-        const float qt = gRq[t], gt = rG2[t];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float x[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int s = half * 32 + i + e;
-            x[e] = s <= t ? tf32r(qt * exp2f(gt - rG2[s]) * rRk[s] * v[i + e]) : 0.f;
-          }
-          *reinterpret_cast<float4*>(sm + L::P32 + kf32(t, half * 32 + i, 64)) = make_float4(x[0], x[1], x[2], x[3]);
-        }
-      }
-    }
-    if (!mbar_wait(bar_mma, mma_ph & 1, kWaitNs)) *abort_flag = 1;
-    ++mma_ph;
+    wait_bar(bar_a, a_ph);
+    wait_bar(bar_b, b_ph);
     tc_fence_after();
+    // V and record part 1 are free: fetch the next chunk's, with its [K;Q] and part 2 into the other buffers
+    __syncthreads();
+    if (tid == 0 && t0 + C < t_end) {
+      load_v_r1(t0 + C, gcur + 1);
+      load_kq_r2(t0 + C, gcur + 1, buf ^ 1);
+    }
     // ---------------------------------------------------------------- W -> tf32 tile
     {
       const int t = 16 * quad + lane;
@@ -516,31 +562,27 @@ __global__ void __launch_bounds__(NT, 1)
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---------------------------------------------------------------- W S0^T (tf32), Q [S0_hi|S0_lo]^T (bf16)
-    if (tid == 0) {
+    // ---------------------------------------------------------------- W S0^T (A, tf32); Q [S0_hi|S0_lo]^T (B, bf16)
+    if (issA) {
       tc_fence_after();
       constexpr uint32_t idw = idesc_tf32(64, R);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint64_t a = sdesc_sw128(sXR + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024);
-        const uint64_t b = sdesc_sw128(sS32 + (j >> 2) * (R * 128) + (j & 3) * 32, 16, 1024);
-        mma_tf32(tmem + L::cD1w, a, b, idw, j > 0);
-      }
-      if (p.write_O) {
-        constexpr uint32_t idq = idesc_bf16(64, R, false, false);
+      for (int j = 0; j < 16; ++j)
+        mma_tf32(tmem + L::cD1w, dadd(dWQ, (j >> 2) * 8192 + (j & 3) * 32),
+                 dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), idw, j > 0);
+      mma_commit(bar_a);
+    } else if (issB && p.write_O) {
+      tc_fence_after();
+      constexpr uint32_t idq = idesc_bf16(64, R, false, false);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t kk = j & 7;  // K step inside d_k; j >= 8 uses the lo half of the state
-          const uint64_t a = sdesc_sw128(sKQ + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sSHL + (j >> 3) * (R * 256) + (kk >> 2) * (R * 128) + (kk & 3) * 32, 16, 1024);
-          mma_bf16(tmem + L::cD1q, a, b, idq, j > 0);
-        }
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t kk = j & 7;  // K step inside d_k; j >= 8 uses the lo half of the state
+        mma_bf16(tmem + L::cD1q, dadd(dKQk, kqo + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                 dadd(dSHL, (j >> 3) * (R * 256) + (kk >> 2) * (R * 128) + (kk & 3) * 32), idq, j > 0);
       }
-      mma_commit(bar_mma);
     }
-    __syncwarp();
-    if (!mbar_wait(bar_mma, mma_ph & 1, kWaitNs)) *abort_flag = 1;
-    ++mma_ph;
+    wait_bar(&bar_r2[buf], r2_ph[buf]);
+    wait_bar(bar_a, a_ph);
     tc_fence_after();
     // ---------------------------------------------------------------- U = U~ - W S0^T; U^ hi/lo (MN-major), U^T (tf32)
     {
@@ -550,7 +592,7 @@ __global__ void __launch_bounds__(NT, 1)
       ld_cols(tmem + lane_base + L::cD1w + half * HALF, dw);
       tmem_ld_wait();
       if (lane < 16) {
-        const float sc = gWsc[t];
+        const float sc = gate[64 + t];
         __align__(16) __nv_bfloat16 hi[HALF], lo[HALF];
 #pragma unroll
         for (int i = 0; i < HALF; ++i) {
@@ -572,66 +614,71 @@ __global__ void __launch_bounds__(NT, 1)
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---------------------------------------------------------------- K^T U^ (state), P U (outputs)
-    if (tid == 0) {
+    // ---------------------------------------------------------------- K^T U^ (A: state); P U (B: outputs)
+    if (issA) {
       tc_fence_after();
       constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        mma_bf16(tmem + L::cD2, sdesc_sw128(sKQ + (j & 3) * 2048, 16384, 1024),
-                 sdesc_sw128(sXR + j * 2048, 16384, 1024), id2, j > 0);
+        mma_bf16(tmem + L::cD2, dadd(dKQmn, kqo + (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, j > 0);
+      mma_commit(bar_a);
+    } else if (issB) {
+      tc_fence_after();
       if (p.write_O) {
         constexpr uint32_t idp = idesc_tf32(64, R);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          mma_tf32(tmem + L::cPU, sdesc_sw128(sP32 + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024),
-                   sdesc_sw128(sXR + 16384 + (j >> 2) * (R * 128) + (j & 3) * 32, 16, 1024), idp, j > 0);
+          mma_tf32(tmem + L::cPU, dadd(dR2, r2o + (j >> 2) * 8192 + (j & 3) * 32),
+                   dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp, j > 0);
       }
-      mma_commit(bar_mma);
+      mma_commit(bar_b);  // covers Q S0^T and P U
     }
-    __syncwarp();
-    if (!mbar_wait(bar_mma, mma_ph & 1, kWaitNs)) *abort_flag = 1;
-    ++mma_ph;
+    wait_bar(bar_a, a_ph);
     tc_fence_after();
-    // ---------------------------------------------------------------- new state; outputs
+    // ---------------------------------------------------------------- new state (tf32 tile first: the next W S0^T needs it)
     {
       float d2[HALF];
       ld_cols(tmem + lane_base + L::cD2 + half * HALF, d2);
       tmem_ld_wait();
-      const float gC = gGam[63];
+      const float gC = gate[63];
 #pragma unroll
       for (int i = 0; i < HALF; ++i) {
         const int c = half * HALF + i;
-        const float s = fmaf(gC, sreg[i], d2[i]);
-        sreg[i] = s;
-        *reinterpret_cast<float*>(sm + L::S32 + kf32(c, dcol, R)) = tf32r(s);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(s);
-        *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + kbf16(c, dcol, R)) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + R * 256 + kbf16(c, dcol, R)) =
-            __float2bfloat16_rn(s - __bfloat162float(hi));
+        sreg[i] = fmaf(gC, sreg[i], d2[i]);
+        *reinterpret_cast<float*>(sm + L::S32 + kf32(c, dcol, R)) = tf32r(sreg[i]);
       }
-      if (p.write_O) {
-        float dq[HALF], pu[HALF];
-        ld_cols(tmem + lane_base + L::cD1q + half * HALF, dq);
-        ld_cols(tmem + lane_base + L::cPU + half * HALF, pu);
-        tmem_ld_wait();
-        const int t = 16 * quad + lane;
-        if (lane < 16 && t < n) {
-          const float gq = gGam[t] * gRq[t];
-          __align__(16) __nv_bfloat16 o[HALF];
+    }
+    wait_bar(bar_b, b_ph);  // Q S0^T has read the bf16 state tile; P U is done
+    tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < HALF; ++i) o[i] = __float2bfloat16_rn(fmaf(gq, dq[i], pu[i]));
-          __nv_bfloat16* dst = p.O + ((size_t)(t0 + t) * p.h_v + h) * DV + row0 + half * HALF;
+    for (int i = 0; i < HALF; ++i) {
+      const int c = half * HALF + i;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(sreg[i]);
+      *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + kbf16(c, dcol, R)) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + R * 256 + kbf16(c, dcol, R)) =
+          __float2bfloat16_rn(sreg[i] - __bfloat162float(hi));
+    }
+    if (p.write_O) {
+      float dq[HALF], pu[HALF];
+      ld_cols(tmem + lane_base + L::cD1q + half * HALF, dq);
+      ld_cols(tmem + lane_base + L::cPU + half * HALF, pu);
+      tmem_ld_wait();
+      const int t = 16 * quad + lane;
+      if (lane < 16 && t < n) {
+        const float gq = gate[128 + t];
+        __align__(16) __nv_bfloat16 o[HALF];
 #pragma unroll
-          for (int i = 0; i < HALF; i += 8)
-            *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
-        }
+        for (int i = 0; i < HALF; ++i) o[i] = __float2bfloat16_rn(fmaf(gq, dq[i], pu[i]));
+        __nv_bfloat16* dst = p.O + ((size_t)(t0 + t) * p.h_v + h) * DV + row0 + half * HALF;
+#pragma unroll
+        for (int i = 0; i < HALF; i += 8)
+          *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) { ok = false; break; }
+    if (flags[0]) { ok = false; break; }
   }
 
   if (!ok && tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
@@ -644,7 +691,7 @@ __global__ void __launch_bounds__(NT, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -689,8 +736,9 @@ cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 }  // namespace
 
 int replay_tc_rows(int n_seqs, int h_v) {
-  // few (tail, head) problems: 4 slices of 32 rows per state to fill the SMs; otherwise 2 slices of 64
-  return (long long)n_seqs * h_v * 4 <= 2 * 152 ? 32 : 64;
+  (void)n_seqs;
+  (void)h_v;
+  return 32;  // 4 slices of 32 state rows per (tail, v-head)
 }
 
 bool replay_tc_supported(const SimtParams& p) {
@@ -716,19 +764,19 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   PrepParams pp;
   pp.g = p.g; pp.beta = p.beta; pp.cu = p.cu; pp.rec = rec; pp.status = p.status;
   pp.n_seqs = p.n_seqs; pp.total_tokens = p.total_tokens; pp.h_k = p.h_k; pp.h_v = p.h_v; pp.l2norm = p.l2norm;
+  pp.write_O = p.write_O; pp.scale = p.scale;
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepLay::ALLOC);
   if (e != cudaSuccess) return e;
   const int chunks_ub = (p.total_tokens + C - 1) / C + p.n_seqs;
-  chunk_prep_kernel<<<dim3(chunks_ub, p.h_k), NT, PrepLay::ALLOC, stream>>>(mk, pp);
+  chunk_prep_kernel<<<dim3(chunks_ub, p.h_k), NT, PrepLay::ALLOC, stream>>>(mq, mk, pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   ScanParams sp;
   sp.cu = p.cu; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
   sp.status = p.status; sp.n_seqs = p.n_seqs; sp.total_tokens = p.total_tokens; sp.h_k = p.h_k; sp.h_v = p.h_v;
-  sp.l2norm = p.l2norm; sp.write_O = p.write_O; sp.scale = p.scale;
-  return replay_tc_rows(p.n_seqs, p.h_v) == 32 ? launch_scan<32>(mq, mk, mv, sp, stream)
-                                               : launch_scan<64>(mq, mk, mv, sp, stream);
+  sp.write_O = p.write_O;
+  return launch_scan<32>(mq, mk, mv, sp, stream);
 }
 
 }  // namespace gdn

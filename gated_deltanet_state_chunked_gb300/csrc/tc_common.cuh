@@ -17,14 +17,16 @@ constexpr int DK = 128, DV = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every barrier wait
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Record of one (chunk, v-head), written by the prep kernel:
-//   [0, 16384)      M = (I + A)^{-1}, fp32 64 x 64 row-major
-//   [16384, 16640)  beta_t (0 past the tail's end)
-//   [16640, 16896)  G_t * log2(e), inclusive gate sums of the chunk
-//   [16896, 17152)  rk_t = 1 / ||k_t|| (1 without normalisation)
-//   [17152, 17408)  unused
-constexpr uint32_t kRecBytes = 17408;
-constexpr uint32_t kRecM = 0, kRecBeta = 16384, kRecG2 = 16640, kRecRk = 16896;
+// Record of one (chunk, v-head), written by the prep kernel and copied verbatim into the
+// scan kernel's shared memory (the tiles are stored as their 128-byte-swizzled images):
+//   [0, 16384)      bf16 [Mb_hi | Mb_lo], Mb = M diag(beta): 2 K-atoms of 64 rows x 128 B
+//   [16384, 24576)  bf16 Mw = M diag(beta gamma rk): 1 K-atom of 64 rows x 128 B
+//   [24576, 40960)  fp32 P (tf32-rounded), P_ts = rq_t rk_s exp(G_t - G_s) q_t.k_s (s <= t): 2 atoms
+//   [40960, 41984)  fp32 gamma_t, rk_t exp(G_last - G_t), gamma_t rq_t, (unused) -- 64 each
+// with M = (I + A)^{-1}.  The scan loads [0, 24576) and [24576, 41984) as two parts.
+constexpr uint32_t kRecMB = 0, kRecMW = 16384, kRecP = 24576, kRecGate = 40960;
+constexpr uint32_t kRecBytes = 41984;
+constexpr uint32_t kRecPart1 = 24576, kRecPart2 = kRecBytes - kRecPart1;
 
 __host__ __device__ inline int chunks_of(int len) { return (len + C - 1) / C; }
 
