@@ -65,6 +65,7 @@ SIGNATURES = {
     "gdn_last_error": ([], ctypes.c_char_p),
     "gdn_workspace_bytes": ([_PD], ctypes.c_size_t),
     "gdn_abi_version": ([], ctypes.c_int),
+    "gdn_set_stage_event": ([_VP], None),
 }
 
 

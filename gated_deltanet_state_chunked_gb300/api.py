@@ -187,3 +187,12 @@ def gdn_workspace_bytes(n_seqs, total_tokens, h_k, h_v, d_k, d_v, dtype=torch.bf
     lib = _lib.load()
     dims = _lib.GdnDims(n_seqs, total_tokens, h_k, h_v, d_k, d_v, _DTYPE[dtype], flags, 1.0)
     return int(lib.gdn_workspace_bytes(ctypes.byref(dims)))
+
+
+def gdn_set_stage_event(event) -> None:
+    """Have this thread's next tensor-core gdn_replay record ``event`` (a
+    torch.cuda.Event) between its prep and scan kernels (measurement hook)."""
+    lib = _lib.load()
+    if event is not None and event.cuda_event == 0:
+        raise ValueError("record-able torch.cuda.Event expected")
+    lib.gdn_set_stage_event(ctypes.c_void_p(event.cuda_event if event is not None else 0))

@@ -13,6 +13,7 @@ namespace gdn {
 namespace {
 
 thread_local std::string g_last_error;
+thread_local void* g_stage_event = nullptr;  // cudaEvent_t to record between prep and scan, once
 
 int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int code, const char* fmt, ...) {
@@ -114,6 +115,12 @@ int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const 
 
 int report_error(int code, const char* message) { return fail(code, "%s", message); }
 
+void* take_stage_event() {
+  void* e = g_stage_event;
+  g_stage_event = nullptr;
+  return e;
+}
+
 int* device_status_word() {
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
@@ -127,6 +134,8 @@ using namespace gdn;
 extern "C" {
 
 int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+void gdn_set_stage_event(void* event) { g_stage_event = event; }
 
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 

@@ -62,5 +62,7 @@ int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const 
                       const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
                       SimtParams* p, bool* nothing_to_do);
 int report_error(int code, const char* message);
+// The event set by gdn_set_stage_event on this thread (nullptr if none); clears it.
+void* take_stage_event();
 
 }  // namespace gdn

@@ -771,6 +771,10 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   chunk_prep_kernel<<<dim3(chunks_ub, p.h_k), NT, PrepLay::ALLOC, stream>>>(mq, mk, pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (void* ev = take_stage_event()) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(ev), stream);
+    if (e != cudaSuccess) return e;
+  }
 
   ScanParams sp;
   sp.cu = p.cu; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;

@@ -174,6 +174,16 @@ const char* gdn_last_error(void);
 /* Bytes of scratch the library's pool needs for this problem (0 if none). */
 size_t gdn_workspace_bytes(const gdn_dims* dims);
 
+/*
+ * gdn_set_stage_event -- measurement hook (no counterpart on the pages).
+ * `event` is a cudaEvent_t created by the caller.  The next gdn_replay or
+ * gdn_replay_noalloc call made by this thread on the tensor-core path records
+ * it on its stream between its two kernels (chunk prep, then scan), so that
+ * the caller can time each kernel with its own events before and after the
+ * call; the hook is then cleared.  Other calls ignore it.
+ */
+void gdn_set_stage_event(void* event);
+
 /* GDN_ABI_VERSION of the loaded library. */
 int gdn_abi_version(void);
 
