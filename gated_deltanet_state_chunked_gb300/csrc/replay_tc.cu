@@ -365,17 +365,18 @@ struct ScanLay {
   static constexpr uint32_t UH = WQ + 32768;        // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
   static constexpr uint32_t UT = UH + 16384;        // fp32 U^T (R rows x 2 atoms)
   static constexpr uint32_t S32 = UT + R * 256;     // fp32 state slice (R rows x 4 atoms), tf32-rounded
-  static constexpr uint32_t SHL = S32 + R * 512;    // bf16 state hi (R rows x 2 atoms), then lo
-  static constexpr uint32_t BARS = SHL + R * 512;
-  static constexpr uint32_t TOTAL = BARS + 128;
+  static constexpr uint32_t SH = S32 + R * 512;     // bf16 state: hi (R rows x 2 atoms), then lo
+  static constexpr uint32_t BARS = SH + R * 512;
+  static constexpr uint32_t TOTAL = BARS + 256;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
   // TMEM columns
-  static constexpr uint32_t cW = 0, cU = 128, cD1w = 128 + R, cD1q = 128 + 2 * R, cD2 = 128 + 3 * R,
-                            cPU = 128 + 4 * R;
-  static constexpr uint32_t TMEM_COLS = (128 + 5 * R) <= 256 ? 256 : 512;
-  static_assert(128 + 5 * R <= 512, "TMEM columns");
+  static constexpr uint32_t cW = 0, cU = 64, cD1w = 64 + 2 * R, cD1q = 64 + 3 * R, cD2 = 64 + 4 * R,
+                            cPU = 64 + 5 * R;
+  static constexpr uint32_t TMEM_COLS = 256;
+  static_assert(64 + 6 * R <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
-  static_assert(R2 % 1024 == 0 && WQ % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 && S32 % 1024 == 0,
+  static_assert(R2 % 1024 == 0 && WQ % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 && S32 % 1024 == 0 &&
+                    SH % 1024 == 0,
                 "tile alignment");
 };
 
@@ -397,35 +398,47 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
-__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
 
 // Advance a shared-memory descriptor's start address by a byte offset (multiple of 16).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
+// Warp-specialised scan.  Warps 0-3 ("chain") carry the state from chunk to chunk and
+// finish each chunk's outputs while its state update is in flight:
+//   D1w = W S0^T -> U = U~ - D1w, U^ -> D2 = K^T U^ (state), P U (outputs) -> S = gamma_C S + D2.
+// Warps 4-7 ("prep") run one chunk ahead: the W^T and U~ MMAs, the tf32 W tile, Q S0^T once
+// the chain has published the chunk's bf16 state, and all loads.  The groups hand over
+// through mbarriers that complete once per chunk; MMAs are issued by several threads in
+// different warps so that independent instruction streams do not queue behind one issuer.
 template <int R>
 __global__ void __launch_bounds__(NT, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, ScanParams p) {
   using L = ScanLay<R>;
-  constexpr int HALF = R / 2;
+  static_assert(R == 32, "one state slice of 32 rows per CTA");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + L::BARS);  // [2]: [K;Q] buffers
-  uint64_t* bar_r2 = bar_kq + 2;                                  // [2]: record part 2 buffers
-  uint64_t* bar_r1 = bar_kq + 4;                                  // V + record part 1
-  uint64_t* bar_a = bar_kq + 5;
-  uint64_t* bar_b = bar_kq + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 56);
-  int* flags = reinterpret_cast<int*>(sm + L::BARS + 60);
-  int* scratch = reinterpret_cast<int*>(sm + L::BARS + 64);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+  uint64_t* bar_kq = bars + 0;   // [2] loads of [K;Q]
+  uint64_t* bar_r2 = bars + 2;   // [2] loads of record part 2
+  uint64_t* bar_r1 = bars + 4;   // V + record part 1
+  uint64_t* bar_w = bars + 5;    // MMA W^T
+  uint64_t* bar_u = bars + 6;    // MMA U~
+  uint64_t* bar_d1 = bars + 7;   // MMA W S0^T
+  uint64_t* bar_d2 = bars + 8;   // MMA K^T U^
+  uint64_t* bar_dq = bars + 9;   // MMA Q S0^T
+  uint64_t* bar_pu = bars + 10;  // MMA P U
+  uint64_t* ev_w = bars + 11;    // prep -> chain: W tile of the chunk ready
+  uint64_t* ev_sh = bars + 12;   // chain -> prep: bf16 state tile of the chunk ready
+  uint64_t* ev_s = bars + 13;    // chain -> prep: chunk finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 128);
+  volatile int* flags = reinterpret_cast<volatile int*>(sm + L::BARS + 132);
+  int* scratch = reinterpret_cast<int*>(sm + L::BARS + 160);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, half = warp >> 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
+  const bool chain = warp < 4;
   const int slice = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int row0 = slice * R;
   const int hk = h / (p.h_v / p.h_k);
-  const bool issA = tid == 0, issB = tid == 128;  // the two MMA-issuing threads
 
   const int t_begin = p.cu[seq], t_end = p.cu[seq + 1];
   if (t_begin < 0 || t_end < t_begin || t_end > p.total_tokens) {
@@ -433,62 +446,65 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
   const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
+  const int nch = chunks_of(t_end - t_begin);
 
   if (warp == 0) {
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
-  auto rec_of = [&](int gc) { return p.rec + ((size_t)gc * p.h_v + h) * kRecBytes; };
-  auto load_kq_r2 = [&](int t0c, int gc, int b) {  // thread 0 only
+  auto rec_of = [&](int c) { return p.rec + ((size_t)(ci.first + c) * p.h_v + h) * kRecBytes; };
+  auto load_kq = [&](int c) {
+    const int b = c & 1, t0c = t_begin + c * C;
     mbar_arrive_expect_tx(&bar_kq[b], 32768);
     for (int a = 0; a < 2; ++a) {
       tma_load_2d(sm + L::KQ + b * 32768 + a * 16384, &map_k, &bar_kq[b], hk * DK + a * 64, t0c);
       tma_load_2d(sm + L::KQ + b * 32768 + a * 16384 + 8192, &map_q, &bar_kq[b], hk * DK + a * 64, t0c);
     }
-    mbar_arrive_expect_tx(&bar_r2[b], kRecPart2);
-    bulk_load(sm + L::R2 + b * 18432, rec_of(gc) + kRecPart1, kRecPart2, &bar_r2[b]);
   };
-  auto load_v_r1 = [&](int t0c, int gc) {  // thread 0 only
+  auto load_r2 = [&](int c) {
+    const int b = c & 1;
+    mbar_arrive_expect_tx(&bar_r2[b], kRecPart2);
+    bulk_load(sm + L::R2 + b * 18432, rec_of(c) + kRecPart1, kRecPart2, &bar_r2[b]);
+  };
+  auto load_r1 = [&](int c) {
     mbar_arrive_expect_tx(bar_r1, 8192 + kRecPart1);
-    tma_load_2d(sm + L::VT, &map_v, bar_r1, h * DV + (row0 & ~63), t0c);
-    bulk_load(sm + L::R1, rec_of(gc), kRecPart1, bar_r1);
+    tma_load_2d(sm + L::VT, &map_v, bar_r1, h * DV + (row0 & ~63), t_begin + c * C);
+    bulk_load(sm + L::R1, rec_of(c), kRecPart1, bar_r1);
   };
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(&bar_kq[i], 1);
+    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
     flags[0] = 0;
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
-    if (t_begin < t_end) {
-      load_kq_r2(t_begin, ci.first, 0);
-      load_v_r1(t_begin, ci.first);
+    if (nch > 0) {
+      load_kq(0);
+      load_r1(0);
+      load_r2(0);
     }
+    if (nch > 1) load_r2(1);
   }
 
-  // entering state: thread owns d = 32*quad + lane and columns [half*HALF, +HALF), fp32 registers
+  // entering state (chain warps): thread owns d = 32*quad + lane and all R columns, fp32 registers
   const int dcol = 32 * quad + lane;
-  float sreg[HALF];
+  float sreg[R];
   const size_t sbase = ((size_t)seq * p.h_v + h) * DV * DK;
+  if (chain) {
 #pragma unroll
-  for (int i = 0; i < HALF; ++i) {
-    const int c = half * HALF + i;
-    const float s = p.S0 ? p.S0[sbase + (size_t)(row0 + c) * DK + dcol] : 0.f;
-    sreg[i] = s;
-    *reinterpret_cast<float*>(sm + L::S32 + kf32(c, dcol, R)) = tf32r(s);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(s);
-    *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + kbf16(c, dcol, R)) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + R * 256 + kbf16(c, dcol, R)) =
-        __float2bfloat16_rn(s - __bfloat162float(hi));
+    for (int c = 0; c < R; ++c) {
+      const float s = p.S0 ? p.S0[sbase + (size_t)(row0 + c) * DK + dcol] : 0.f;
+      sreg[c] = s;
+      *reinterpret_cast<float*>(sm + L::S32 + kf32(c, dcol, R)) = tf32r(s);
+    }
+    fence_async_smem();
   }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const uint32_t vcoloff = (uint32_t)(row0 & 63) * 2u;
-  // base descriptors (start address advanced per K step with dadd)
   const uint64_t dKQk = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);      // K-major view of [K;Q]
   const uint64_t dKQmn = sdesc_sw128(smem_u32(sm + L::KQ), 16384, 1024);  // MN-major view of K
   const uint64_t dVT = sdesc_sw128(smem_u32(sm + L::VT) + vcoloff, 8192, 1024);
@@ -498,196 +514,202 @@ __global__ void __launch_bounds__(NT, 1)
   const uint64_t dUHmn = sdesc_sw128(smem_u32(sm + L::UH), 16384, 1024);
   const uint64_t dUT = sdesc_sw128(smem_u32(sm + L::UT), 16, 1024);
   const uint64_t dS32 = sdesc_sw128(smem_u32(sm + L::S32), 16, 1024);
-  const uint64_t dSHL = sdesc_sw128(smem_u32(sm + L::SHL), 16, 1024);
-  uint32_t kq_ph[2] = {0, 0}, r2_ph[2] = {0, 0}, r1_ph = 0, a_ph = 0, b_ph = 0;
-  bool ok = true;
-  auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
-    if (!mbar_wait(bar, ph & 1, kWaitNs)) flags[0] = 1;
-    ++ph;
+  const uint64_t dSH = sdesc_sw128(smem_u32(sm + L::SH), 16, 1024);
+  // Bounded wait.  After the first timeout every later wait returns at once, so both
+  // warp groups run their (uniform) loops to the end and the CTA exits with an error.
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (flags[0]) return;
+    if (!mbar_wait(bar, parity, kWaitNs)) flags[0] = 1;
   };
-  int gcur = ci.first;
-  int buf = 0;
 
-  for (int t0 = t_begin; t0 < t_end; t0 += C, ++gcur, buf ^= 1) {
-    const int n = min(C, t_end - t0);
-    const uint32_t kqo = (uint32_t)buf * 32768u, r2o = (uint32_t)buf * 18432u;
-    const float* gate = reinterpret_cast<const float*>(sm + L::R2 + r2o + (kRecGate - kRecPart1));
-    wait_bar(&bar_kq[buf], kq_ph[buf]);
-    wait_bar(bar_r1, r1_ph);
-    __syncthreads();
-    if (flags[0]) { ok = false; break; }
-    // ---------------------------------------------------------------- W = Mw K (A), U~ = Mb V (B)
-    if (issA) {
+  if (chain) {
+    // ============================================================ chain warps
+    const int t = 16 * quad + lane;  // M=64 layout row (lanes 0-15)
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t par = c & 1;
+      const float* gate = reinterpret_cast<const float*>(sm + L::R2 + par * 18432 + (kRecGate - kRecPart1));
+      wait(ev_w, par);
+      if (tid == 0) {  // D1w = W S0^T (tf32)
+        tc_fence_after();
+        constexpr uint32_t idw = idesc_tf32(64, R);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          mma_tf32(tmem + L::cD1w, dadd(dWQ, (j >> 2) * 8192 + (j & 3) * 32),
+                   dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), idw, j > 0);
+        mma_commit(bar_d1);
+      }
+      if (p.write_O) {  // bf16 hi|lo copy of the entering state for Q S0^T (its last reader: Q S0^T of c-1)
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(sreg[i]);
+          *reinterpret_cast<__nv_bfloat16*>(sm + L::SH + kbf16(i, dcol, R)) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(sm + L::SH + R * 256 + kbf16(i, dcol, R)) =
+              __float2bfloat16_rn(sreg[i] - __bfloat162float(hi));
+        }
+        fence_async_smem();
+        group_sync(1);
+        if (tid == 0) mbar_arrive(ev_sh);
+      }
+      wait(bar_r2 + par, (c >> 1) & 1);  // factors and P of this chunk
+      wait(bar_d1, par);
       tc_fence_after();
-      constexpr uint32_t idW = idesc_bf16(64, 128, false, true);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mma_bf16(tmem + L::cW, dadd(dR1, kRecMW + j * 32), dadd(dKQmn, kqo + j * 2048), idW, j > 0);
-      mma_commit(bar_a);
-    } else if (issB) {
-      tc_fence_after();
-      constexpr uint32_t idU = idesc_bf16(64, R, false, true);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma_bf16(tmem + L::cU, dadd(dR1, kRecMB + (j >> 2) * 8192 + (j & 3) * 32), dadd(dVT, (j & 3) * 2048), idU,
-                 j > 0);
-      mma_commit(bar_b);
-    }
-    wait_bar(bar_a, a_ph);
-    wait_bar(bar_b, b_ph);
-    tc_fence_after();
-    // V and record part 1 are free: fetch the next chunk's, with its [K;Q] and part 2 into the other buffers
-    __syncthreads();
-    if (tid == 0 && t0 + C < t_end) {
-      load_v_r1(t0 + C, gcur + 1);
-      load_kq_r2(t0 + C, gcur + 1, buf ^ 1);
-    }
-    // ---------------------------------------------------------------- W -> tf32 tile
-    {
-      const int t = 16 * quad + lane;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float v[32];
-        const int d0 = half * 64 + cc * 32;
-        ld_cols(tmem + lane_base + L::cW + d0, v);
+      {  // U = U~ - W S0^T (M=64 layout); U^ hi|lo MN-major, U^T tf32
+        float ut[R], dw[R];
+        tmem_ld32(tmem + lane_base + L::cU + par * R, ut);
+        tmem_ld32(tmem + lane_base + L::cD1w, dw);
         tmem_ld_wait();
         if (lane < 16) {
+          const float sc = gate[64 + t];
+          __align__(16) __nv_bfloat16 hi[R], lo[R];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(sm + L::WQ + kf32(t, d0 + i, 64)) =
-                make_float4(tf32r(v[i]), tf32r(v[i + 1]), tf32r(v[i + 2]), tf32r(v[i + 3]));
+          for (int i = 0; i < R; i += 4) {
+            float u4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float u = ut[i + e] - dw[i + e];
+              u4[e] = tf32r(u);
+              const float uh = u * sc;
+              hi[i + e] = __float2bfloat16_rn(uh);
+              lo[i + e] = __float2bfloat16_rn(uh - __bfloat162float(hi[i + e]));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) *reinterpret_cast<float*>(sm + L::UT + kf32(i + e, t, R)) = u4[e];
+          }
+#pragma unroll
+          for (int i = 0; i < R; i += 8) {
+            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 128)) = *reinterpret_cast<const uint4*>(hi + i);
+            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lo + i);
+          }
         }
       }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---------------------------------------------------------------- W S0^T (A, tf32); Q [S0_hi|S0_lo]^T (B, bf16)
-    if (issA) {
-      tc_fence_after();
-      constexpr uint32_t idw = idesc_tf32(64, R);
+      fence_async_smem();
+      tc_fence_before();
+      group_sync(1);
+      if (tid == 0) {  // K^T U^ (state)
+        tc_fence_after();
+        constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
+        const uint32_t kqo = par * 32768u;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        mma_tf32(tmem + L::cD1w, dadd(dWQ, (j >> 2) * 8192 + (j & 3) * 32),
-                 dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), idw, j > 0);
-      mma_commit(bar_a);
-    } else if (issB && p.write_O) {
-      tc_fence_after();
-      constexpr uint32_t idq = idesc_bf16(64, R, false, false);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t kk = j & 7;  // K step inside d_k; j >= 8 uses the lo half of the state
-        mma_bf16(tmem + L::cD1q, dadd(dKQk, kqo + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32),
-                 dadd(dSHL, (j >> 3) * (R * 256) + (kk >> 2) * (R * 128) + (kk & 3) * 32), idq, j > 0);
-      }
-    }
-    wait_bar(&bar_r2[buf], r2_ph[buf]);
-    wait_bar(bar_a, a_ph);
-    tc_fence_after();
-    // ---------------------------------------------------------------- U = U~ - W S0^T; U^ hi/lo (MN-major), U^T (tf32)
-    {
-      const int t = 16 * quad + lane;
-      float ut[HALF], dw[HALF];
-      ld_cols(tmem + lane_base + L::cU + half * HALF, ut);
-      ld_cols(tmem + lane_base + L::cD1w + half * HALF, dw);
-      tmem_ld_wait();
-      if (lane < 16) {
-        const float sc = gate[64 + t];
-        __align__(16) __nv_bfloat16 hi[HALF], lo[HALF];
-#pragma unroll
-        for (int i = 0; i < HALF; ++i) {
-          const float u = ut[i] - dw[i];
-          const int c = half * HALF + i;
-          *reinterpret_cast<float*>(sm + L::UT + kf32(c, t, R)) = tf32r(u);
-          const float uh = u * sc;
-          hi[i] = __float2bfloat16_rn(uh);
-          lo[i] = __float2bfloat16_rn(uh - __bfloat162float(hi[i]));
-        }
-#pragma unroll
-        for (int i = 0; i < HALF; i += 8) {
-          const int c = half * HALF + i;
-          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(c, t, 128)) = *reinterpret_cast<const uint4*>(hi + i);
-          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(c, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lo + i);
-        }
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---------------------------------------------------------------- K^T U^ (A: state); P U (B: outputs)
-    if (issA) {
-      tc_fence_after();
-      constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma_bf16(tmem + L::cD2, dadd(dKQmn, kqo + (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, j > 0);
-      mma_commit(bar_a);
-    } else if (issB) {
-      tc_fence_after();
-      if (p.write_O) {
+        for (int j = 0; j < 8; ++j)
+          mma_bf16(tmem + L::cD2, dadd(dKQmn, kqo + (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, j > 0);
+        mma_commit(bar_d2);
+      } else if (tid == 32 && p.write_O) {  // P U (outputs)
+        tc_fence_after();
         constexpr uint32_t idp = idesc_tf32(64, R);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          mma_tf32(tmem + L::cPU, dadd(dR2, r2o + (j >> 2) * 8192 + (j & 3) * 32),
+          mma_tf32(tmem + L::cPU, dadd(dR2, par * 18432 + (j >> 2) * 8192 + (j & 3) * 32),
                    dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp, j > 0);
+        mma_commit(bar_pu);
       }
-      mma_commit(bar_b);  // covers Q S0^T and P U
-    }
-    wait_bar(bar_a, a_ph);
-    tc_fence_after();
-    // ---------------------------------------------------------------- new state (tf32 tile first: the next W S0^T needs it)
-    {
-      float d2[HALF];
-      ld_cols(tmem + lane_base + L::cD2 + half * HALF, d2);
-      tmem_ld_wait();
-      const float gC = gate[63];
+      if (p.write_O) {  // outputs of chunk c while K^T U^ runs
+        wait(bar_pu, par);
+        wait(bar_dq, par);
+        tc_fence_after();
+        float dq[R], pu[R];
+        tmem_ld32(tmem + lane_base + L::cD1q, dq);
+        tmem_ld32(tmem + lane_base + L::cPU, pu);
+        tmem_ld_wait();
+        const int t0c = t_begin + c * C, n = min(C, t_end - t0c);
+        if (lane < 16 && t < n) {
+          const float gq = gate[128 + t];
+          __align__(16) __nv_bfloat16 o[R];
 #pragma unroll
-      for (int i = 0; i < HALF; ++i) {
-        const int c = half * HALF + i;
-        sreg[i] = fmaf(gC, sreg[i], d2[i]);
-        *reinterpret_cast<float*>(sm + L::S32 + kf32(c, dcol, R)) = tf32r(sreg[i]);
+          for (int i = 0; i < R; ++i) o[i] = __float2bfloat16_rn(fmaf(gq, dq[i], pu[i]));
+          __nv_bfloat16* dst = p.O + ((size_t)(t0c + t) * p.h_v + h) * DV + row0;
+#pragma unroll
+          for (int i = 0; i < R; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
+        }
+      }
+      wait(bar_d2, par);
+      tc_fence_after();
+      {  // S <- gamma_C S + K^T U^ (M=128 layout: lane = d_k)
+        float d2[R];
+        tmem_ld32(tmem + lane_base + L::cD2, d2);
+        tmem_ld_wait();
+        const float gC = gate[63];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          sreg[i] = fmaf(gC, sreg[i], d2[i]);
+          *reinterpret_cast<float*>(sm + L::S32 + kf32(i, dcol, R)) = tf32r(sreg[i]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      group_sync(1);
+      if (tid == 0) mbar_arrive(ev_s);
+    }
+  } else {
+    // ============================================================ prep warps
+    const bool issW = tid == 128, issU = tid == 192, issQ = tid == 224;
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t par = c & 1;
+      wait(bar_kq + par, (c >> 1) & 1);
+      wait(bar_r1, par);
+      if (issW) {  // W^T = K^T Mw^T (M=128 over d_k, N=64 tokens)
+        tc_fence_after();
+        constexpr uint32_t idW = idesc_bf16(128, 64, true, false);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16(tmem + L::cW, dadd(dKQmn, par * 32768 + j * 2048), dadd(dR1, kRecMW + j * 32), idW, j > 0);
+        mma_commit(bar_w);
+      } else if (issU) {  // U~ = [Mb_hi|Mb_lo][V;V]
+        tc_fence_after();
+        constexpr uint32_t idU = idesc_bf16(64, R, false, true);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          mma_bf16(tmem + L::cU + par * R, dadd(dR1, kRecMB + (j >> 2) * 8192 + (j & 3) * 32),
+                   dadd(dVT, (j & 3) * 2048), idU, j > 0);
+        mma_commit(bar_u);
+      }
+      wait(bar_w, par);
+      wait(bar_u, par);
+      tc_fence_after();
+      group_sync(2);
+      if (issU && c + 1 < nch) load_r1(c + 1);   // V and record part 1 are free
+      if (c > 0) wait(bar_d1, (c - 1) & 1);       // the previous W S0^T has read the W tile
+      {  // W^T (M=128 layout: lane = d_k) -> tf32 tile W[t][d]
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + L::cW + cc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) *reinterpret_cast<float*>(sm + L::WQ + kf32(cc * 32 + i, dcol, 64)) = tf32r(v[i]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      if (c > 0) wait(ev_s, (c - 1) & 1);  // the chain has finished chunk c-1
+      group_sync(2);
+      if (issW) mbar_arrive(ev_w);
+      if (issU && c + 1 < nch) {           // buffers of chunk c-1 have no readers left
+        load_kq(c + 1);
+        if (c >= 1) load_r2(c + 1);
+      }
+      if (p.write_O) {
+        wait(ev_sh, par);
+        if (issQ) {  // Q [S0_hi|S0_lo]^T (bf16) of chunk c
+          tc_fence_after();
+          constexpr uint32_t idq = idesc_bf16(64, R, false, false);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t kk = j & 7;  // K step inside d_k; j >= 8 uses the lo half of the state
+            mma_bf16(tmem + L::cD1q, dadd(dKQk, par * 32768 + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                     dadd(dSH, (j >> 3) * (R * 256) + (kk >> 2) * (R * 128) + (kk & 3) * 32), idq, j > 0);
+          }
+          mma_commit(bar_dq);
+        }
       }
     }
-    wait_bar(bar_b, b_ph);  // Q S0^T has read the bf16 state tile; P U is done
-    tc_fence_after();
-#pragma unroll
-    for (int i = 0; i < HALF; ++i) {
-      const int c = half * HALF + i;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(sreg[i]);
-      *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + kbf16(c, dcol, R)) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(sm + L::SHL + R * 256 + kbf16(c, dcol, R)) =
-          __float2bfloat16_rn(sreg[i] - __bfloat162float(hi));
-    }
-    if (p.write_O) {
-      float dq[HALF], pu[HALF];
-      ld_cols(tmem + lane_base + L::cD1q + half * HALF, dq);
-      ld_cols(tmem + lane_base + L::cPU + half * HALF, pu);
-      tmem_ld_wait();
-      const int t = 16 * quad + lane;
-      if (lane < 16 && t < n) {
-        const float gq = gate[128 + t];
-        __align__(16) __nv_bfloat16 o[HALF];
-#pragma unroll
-        for (int i = 0; i < HALF; ++i) o[i] = __float2bfloat16_rn(fmaf(gq, dq[i], pu[i]));
-        __nv_bfloat16* dst = p.O + ((size_t)(t0 + t) * p.h_v + h) * DV + row0 + half * HALF;
-#pragma unroll
-        for (int i = 0; i < HALF; i += 8)
-          *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (flags[0]) { ok = false; break; }
   }
 
-  if (!ok && tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
-  if (ok) {
+  __syncthreads();
+  if (flags[0]) {
+    if (tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
+  } else if (chain) {
 #pragma unroll
-    for (int i = 0; i < HALF; ++i) {
-      const int c = half * HALF + i;
-      p.S_out[sbase + (size_t)(row0 + c) * DK + dcol] = sreg[i];
-    }
+    for (int c = 0; c < R; ++c) p.S_out[sbase + (size_t)(row0 + c) * DK + dcol] = sreg[c];
   }
   tc_fence_before();
   __syncthreads();
