@@ -8,6 +8,8 @@
 // independently, so one CTA owns a 32-row slice of one head's state and walks
 // the K steps, staging T_j in shared memory.
 #include "gdn_internal.cuh"
+#include "tc_common.cuh"
+#include "umma.cuh"
 
 namespace gdn {
 namespace {
@@ -62,9 +64,125 @@ __global__ void __launch_bounds__(NT) compose_simt_kernel(ComposeParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// d_k = d_v = 128: register-tiled kernel.  One CTA owns 32 rows of one head's state (kept in
+// shared memory) and walks the K steps.  T_j (64 KB, contiguous) and S_local_j's 32-row slice
+// arrive by bulk copies two steps ahead of use.  Thread (r, g) computes row r, columns g + 8 i
+// (i < 16) of S T_j^T with float4 shared loads, walking k in an order rotated by 4 g so that
+// the eight column groups of a warp read eight different 16-byte chunks of their T rows.
+constexpr int CR = 32, CNT = 256, CPAD = 132, CD = 128;
+struct CLay {
+  static constexpr uint32_t TB = 0;                       // 2 x T_j [128][128] fp32
+  static constexpr uint32_t TBYTES = CD * CD * 4;         // 65536
+  static constexpr uint32_t SS = 2 * TBYTES;              // S slice [32][132]
+  static constexpr uint32_t LB = SS + CR * CPAD * 4;      // 2 x S_local slice [32][128]
+  static constexpr uint32_t BARS = LB + 2 * CR * CD * 4;  // bar_t[2], bar_l[2], abort flag
+  static constexpr uint32_t TOTAL = BARS + 64;
+};
+
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+__global__ void __launch_bounds__(CNT, 1) compose_tiled_kernel(ComposeParams p) {
+  using L = CLay;
+  extern __shared__ __align__(16) unsigned char cmem[];
+  float* Sx = reinterpret_cast<float*>(cmem + L::SS);
+  uint64_t* bar_t = reinterpret_cast<uint64_t*>(cmem + L::BARS);
+  uint64_t* bar_l = bar_t + 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(cmem + L::BARS + 32);
+  const int tid = threadIdx.x, lane = tid & 31, r = tid >> 3, g = tid & 7;
+  const int h = blockIdx.y, row0 = blockIdx.x * CR;
+  const size_t sbase = (size_t)h * CD * CD;
+
+  auto issue_t = [&](int j) {  // warp 0
+    unsigned char* dst = cmem + L::TB + (j & 1) * L::TBYTES;
+    if (lane == 0) {
+      tc::mbar_arrive_expect_tx(&bar_t[j & 1], CD * CD * 4);
+      const float* src = p.T[j] + sbase;
+      bulk_copy(dst, src, CD * CD * 2, &bar_t[j & 1]);
+      bulk_copy(dst + CD * CD * 2, src + CD * CD / 2, CD * CD * 2, &bar_t[j & 1]);
+    }
+  };
+  auto issue_l = [&](int j) {  // one thread
+    tc::mbar_arrive_expect_tx(&bar_l[j & 1], CR * CD * 4);
+    bulk_copy(cmem + L::LB + (j & 1) * (CR * CD * 4), p.Slocal[j] + sbase + (size_t)row0 * CD, CR * CD * 4,
+              &bar_l[j & 1]);
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (*abort_flag) return;
+    if (!tc::mbar_wait(bar, parity, tcp::kWaitNs)) *abort_flag = 1;
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&bar_t[i], 1);
+    tc::mbar_fence_init();
+    *abort_flag = 0;
+  }
+  for (int i = tid; i < CR * CD; i += CNT) {
+    const int rr = i / CD, d = i % CD;
+    Sx[rr * CPAD + d] = p.S_in ? p.S_in[sbase + (size_t)(row0 + rr) * CD + d] : 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    for (int j = 0; j < 2 && j < p.K; ++j) {
+      issue_t(j);
+      if (lane == 0) issue_l(j);
+    }
+  }
+  for (int j = 0; j < p.K; ++j) {
+    const uint32_t par = (j >> 1) & 1;
+    const float* Tb = reinterpret_cast<const float*>(cmem + L::TB + (j & 1) * L::TBYTES);
+    wait(&bar_t[j & 1], par);
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    const float* srow = Sx + r * CPAD;
+#pragma unroll 4
+    for (int q = 0; q < CD / 4; ++q) {
+      const int kk = ((q + g) & (CD / 4 - 1)) * 4;
+      const float4 s4 = *reinterpret_cast<const float4*>(srow + kk);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 t4 = *reinterpret_cast<const float4*>(Tb + (g + 8 * i) * CD + kk);
+        acc[i] = fmaf(s4.x, t4.x, acc[i]);
+        acc[i] = fmaf(s4.y, t4.y, acc[i]);
+        acc[i] = fmaf(s4.z, t4.z, acc[i]);
+        acc[i] = fmaf(s4.w, t4.w, acc[i]);
+      }
+    }
+    __syncthreads();  // every read of the state slice and of T_j is done
+    if (tid < 32 && j + 2 < p.K) issue_t(j + 2);
+    wait(&bar_l[j & 1], par);
+    const float* Lb = reinterpret_cast<const float*>(cmem + L::LB + (j & 1) * (CR * CD * 4));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Sx[r * CPAD + g + 8 * i] = acc[i] + Lb[r * CD + g + 8 * i];
+    __syncthreads();  // the new state slice is complete; S_local_j's buffer is free
+    if (tid == 0 && j + 2 < p.K) issue_l(j + 2);
+  }
+  if (*abort_flag) {
+    if (tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
+    return;
+  }
+  for (int i = tid; i < CR * CD; i += CNT) {
+    const int rr = i / CD, d = i % CD;
+    p.S_out[sbase + (size_t)(row0 + rr) * CD + d] = Sx[rr * CPAD + d];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_compose_simt(const ComposeParams& p, cudaStream_t stream) {
+  if (p.d_k == CD && p.d_v == CD) {
+    cudaError_t e = cudaFuncSetAttribute(compose_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)CLay::TOTAL);
+    if (e != cudaSuccess) return e;
+    compose_tiled_kernel<<<dim3(CD / CR, p.h), CNT, CLay::TOTAL, stream>>>(p);
+    return cudaGetLastError();
+  }
   dim3 grid((p.d_v + RS - 1) / RS, p.h);
   const size_t smem = sizeof(float) * (size_t)(kMaxHead + RS) * TST;
   cudaError_t e = cudaFuncSetAttribute(compose_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -49,6 +49,7 @@ struct ComposeParams {
   const float* Slocal[kMaxCompose];
   const float* S_in;
   float* S_out;
+  int* status;  // sticky device status word (bounded waits that give up report GDN_ERR_TIMEOUT)
   int K, h, d_k, d_v;
 };
 
