@@ -67,10 +67,11 @@ __global__ void __launch_bounds__(NT) compose_simt_kernel(ComposeParams p) {
 // ---------------------------------------------------------------------------------------------
 // d_k = d_v = 128: register-tiled kernel.  One CTA owns 32 rows of one head's state (kept in
 // shared memory) and walks the K steps.  T_j (64 KB, contiguous) and S_local_j's 32-row slice
-// arrive by bulk copies two steps ahead of use.  Thread (r, g) computes row r, columns g + 8 i
-// (i < 16) of S T_j^T with float4 shared loads, walking k in an order rotated by 4 g so that
-// the eight column groups of a warp read eight different 16-byte chunks of their T rows.
-constexpr int CR = 32, CNT = 256, CPAD = 132, CD = 128;
+// arrive by bulk copies two steps ahead of use.  Thread (b, g) computes rows 4 b .. 4 b + 3 and
+// columns g + 16 i (i < 8) of S T_j^T with float4 shared loads (each loaded T value feeds four
+// rows, each S value eight columns), walking k in an order rotated by 4 g so that the eight
+// threads of a quarter warp read eight different 16-byte chunks of their T and S rows.
+constexpr int CR = 32, CNT = 128, CPAD = 132, CD = 128;
 struct CLay {
   static constexpr uint32_t TB = 0;                       // 2 x T_j [128][128] fp32
   static constexpr uint32_t TBYTES = CD * CD * 4;         // 65536
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(CNT, 1) compose_tiled_kernel(ComposeParams p) 
   uint64_t* bar_t = reinterpret_cast<uint64_t*>(cmem + L::BARS);
   uint64_t* bar_l = bar_t + 2;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cmem + L::BARS + 32);
-  const int tid = threadIdx.x, lane = tid & 31, r = tid >> 3, g = tid & 7;
+  const int tid = threadIdx.x, lane = tid & 31, rb = 4 * (tid >> 4), g = tid & 15;
   const int h = blockIdx.y, row0 = blockIdx.x * CR;
   const size_t sbase = (size_t)h * CD * CD;
 
@@ -137,29 +138,38 @@ __global__ void __launch_bounds__(CNT, 1) compose_tiled_kernel(ComposeParams p) 
     const uint32_t par = (j >> 1) & 1;
     const float* Tb = reinterpret_cast<const float*>(cmem + L::TB + (j & 1) * L::TBYTES);
     wait(&bar_t[j & 1], par);
-    float acc[16];
+    float acc[4][8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    const float* srow = Sx + r * CPAD;
-#pragma unroll 4
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[a][i] = 0.f;
+#pragma unroll 2
     for (int q = 0; q < CD / 4; ++q) {
       const int kk = ((q + g) & (CD / 4 - 1)) * 4;
-      const float4 s4 = *reinterpret_cast<const float4*>(srow + kk);
+      float4 s4[4], t4[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 t4 = *reinterpret_cast<const float4*>(Tb + (g + 8 * i) * CD + kk);
-        acc[i] = fmaf(s4.x, t4.x, acc[i]);
-        acc[i] = fmaf(s4.y, t4.y, acc[i]);
-        acc[i] = fmaf(s4.z, t4.z, acc[i]);
-        acc[i] = fmaf(s4.w, t4.w, acc[i]);
-      }
+      for (int a = 0; a < 4; ++a) s4[a] = *reinterpret_cast<const float4*>(Sx + (rb + a) * CPAD + kk);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t4[i] = *reinterpret_cast<const float4*>(Tb + (g + 16 * i) * CD + kk);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[a][i] = fmaf(s4[a].x, t4[i].x, acc[a][i]);
+          acc[a][i] = fmaf(s4[a].y, t4[i].y, acc[a][i]);
+          acc[a][i] = fmaf(s4[a].z, t4[i].z, acc[a][i]);
+          acc[a][i] = fmaf(s4[a].w, t4[i].w, acc[a][i]);
+        }
     }
     __syncthreads();  // every read of the state slice and of T_j is done
     if (tid < 32 && j + 2 < p.K) issue_t(j + 2);
     wait(&bar_l[j & 1], par);
     const float* Lb = reinterpret_cast<const float*>(cmem + L::LB + (j & 1) * (CR * CD * 4));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Sx[r * CPAD + g + 8 * i] = acc[i] + Lb[r * CD + g + 8 * i];
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        Sx[(rb + a) * CPAD + g + 16 * i] = acc[a][i] + Lb[(rb + a) * CD + g + 16 * i];
     __syncthreads();  // the new state slice is complete; S_local_j's buffer is free
     if (tid == 0 && j + 2 < p.K) issue_l(j + 2);
   }
