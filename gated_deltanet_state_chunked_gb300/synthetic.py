@@ -190,3 +190,13 @@ def varlen_workload_inputs(layer: int, n_tails: int = 64, h_k: int = 16, h_v: in
     seed = config_seed(2, layer)
     lengths = varlen_tail_lengths(n_tails, seed)
     return make_replay_inputs(lengths, h_k, h_v, d, d, dtype=dtype, seed=seed)
+
+
+def chunk_workload_inputs(layer: int = 0, n_chunks: int = 16, chunk_len: int = 2048, h_k: int = 16, h_v: int = 32,
+                          d: int = 128, weak_decay: bool = False) -> ReplayInputs:
+    """Isolated chunks of one layer for the chunk-operator / composition workload: ``n_chunks``
+    chunks of ``chunk_len`` tokens in fp32, each chunk its own sequence of cu_seqlens.
+    ``weak_decay`` scales the gates by 1e-3 instead of 0.1, so that the chunk transitions T_C do
+    not underflow to zero in fp32."""
+    return make_replay_inputs([chunk_len] * n_chunks, h_k, h_v, d, d, dtype="f32", seed=config_seed(3, layer),
+                              gate_scale=1e-3 if weak_decay else 0.1)
