@@ -47,6 +47,7 @@ def parse_args():
     ap.add_argument("--precise", action="store_true", help="bf16 inputs on the fp32 CUDA-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the varlen / full / chunk-operator / compose rows")
     return ap.parse_args()
 
 
@@ -230,6 +231,101 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _timed_us(fn, flush, reps, warmup=2):
+    """Median device time of fn() in microseconds, L2 flushed before every call."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return float(np.median(ts))
+
+
+def measure_rows(dev, flush, peaks, replay_us):
+    """The other measured workloads: the varlen layer, the full 32K prefix against its 10% tail,
+    and the chunk operators and composition of 16 isolated 2048-token chunks."""
+    import torch
+
+    from gated_deltanet_state_chunked_gb300 import api, synthetic
+    import oracle
+
+    def dev_inputs(x):
+        dt = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+        f = lambda a, d: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(d)
+        return dict(q=f(x.q, dt), k=f(x.k, dt), v=f(x.v, dt), g=f(x.g, torch.float32),
+                    beta=f(x.beta, torch.float32), cu=f(x.cu_seqlens, torch.int32))
+
+    rows = {}
+    hbm = peaks["hbm_gbs"]
+    # varlen layer: 64 tails of one layer
+    x = synthetic.varlen_workload_inputs(0)
+    d = dev_inputs(x)
+    O = torch.empty((x.total_tokens, x.h_v, x.d_v), dtype=torch.bfloat16, device=dev)
+    S = torch.empty((x.n_seqs, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    us = _timed_us(lambda: api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], O_out=O, S_out=S),
+                   flush, 5)
+    fl, by = algorithmic(x, with_O=True)
+    rows["varlen_layer"] = {"tails": x.n_seqs, "tokens": x.total_tokens, "us": us,
+                            "tokens_per_s": x.total_tokens / (us * 1e-6), "hbm_frac": by / (us * 1e-6) / 1e9 / hbm,
+                            "algorithmic_bytes": by, "algorithmic_flops": fl}
+    del d, O, S
+    # full 32K prefix vs its last 3277 tokens replayed from a zero state (config gates, then weak decay)
+    for tag, gs in (("full_32k", 0.1), ("full_32k_weak_decay", 1e-3)):
+        x = synthetic.workload_inputs("full_32k", gate_scale=gs)
+        d = dev_inputs(x)
+        S_full = torch.empty((1, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        S_tail = torch.empty_like(S_full)
+        r = 3277
+        cu_tail = torch.tensor([0, r], dtype=torch.int32, device=dev)
+        tail = {n: d[n][-r:].contiguous() for n in ("q", "k", "v", "g", "beta")}
+        full_fn = lambda: api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], S_out=S_full,
+                                         state_only=True)
+        tail_fn = lambda: api.gdn_replay(tail["q"], tail["k"], tail["v"], tail["g"], tail["beta"], cu_tail,
+                                         S_out=S_tail, state_only=True)
+        full_us = _timed_us(full_fn, flush, 3) if tag == "full_32k" else None
+        full_fn()
+        tail_fn()
+        torch.cuda.synchronize()
+        err = oracle.rel_err(S_tail.double().cpu().numpy(), S_full.double().cpu().numpy())
+        ent = {"replay_vs_full_rel_err_S": err, "tail_tokens": r, "gate_scale": gs}
+        if full_us is not None:
+            ent |= {"full_us_state_only": full_us, "replay_us_with_outputs": replay_us,
+                    "speedup_full_over_replay": full_us / replay_us}
+        rows[tag] = ent
+        del d, tail
+    # chunk operators of 16 x 2048 fp32 chunks and their composition (K = 16, 32 heads, d = 128)
+    x = synthetic.chunk_workload_inputs()
+    d = dev_inputs(x)
+    K = x.n_seqs
+    T = torch.empty((K, x.h_v, x.d_k, x.d_k), dtype=torch.float32, device=dev)
+    Sl = torch.empty((K, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    us = _timed_us(lambda: api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], d["cu"], T_out=T, Slocal_out=Sl),
+                   flush, 2, warmup=1)
+    rows_aug = x.d_v + x.d_k
+    fl = x.total_tokens * x.h_v * (6 * x.d_k * rows_aug + 64 * (6 * x.d_k + 4 * rows_aug))
+    rows["chunk_operator"] = {"chunks": K, "chunk_tokens": 2048, "heads": x.h_v, "dtype": "f32", "us": us,
+                              "algorithmic_flops": fl, "tflops": fl / (us * 1e-6) / 1e12,
+                              "path": "fp32 CUDA cores"}
+    Tl, Sll = [T[j] for j in range(K)], [Sl[j] for j in range(K)]
+    SK = torch.empty((x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    us = _timed_us(lambda: api.gdn_compose(Tl, Sll, None, S_out=SK), flush, 10)
+    by = K * x.h_v * (x.d_k * x.d_k + x.d_v * x.d_k) * 4 + x.h_v * x.d_v * x.d_k * 4
+    fl = K * x.h_v * 2 * x.d_v * x.d_k * x.d_k
+    rows["compose"] = {"K": K, "heads": x.h_v, "d": x.d_k, "us": us, "algorithmic_bytes": by,
+                       "gbs": by / (us * 1e-6) / 1e9, "hbm_frac": by / (us * 1e-6) / 1e9 / hbm,
+                       "algorithmic_flops": fl, "path": "fp32 CUDA cores"}
+    api.gdn_get_status()
+    return rows
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -373,6 +469,9 @@ def run_ours(args):
         return
     flops, byts = algorithmic(x, with_O=True)
     peaks, peak_src = load_peaks()
+    rows = None
+    if world == 1 and not args.no_rows:
+        rows = measure_rows(dev, flush, peaks, ms * 1e3)
     t_s = ms * 1e-3
     gbs = byts / t_s / 1e9
     tfs = flops / t_s / 1e12
@@ -394,7 +493,7 @@ def run_ours(args):
                                                 "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps * (2 if tensor_path else 1),
-        "clocks": clocks, "parity": parity,
+        "clocks": clocks, "parity": parity, "rows": rows,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
