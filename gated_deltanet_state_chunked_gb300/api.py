@@ -86,7 +86,7 @@ def gdn_replay_noalloc(q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, *, l2norm
     Same arguments and results as gdn_replay, except that the outputs O_out
     (None with ``state_only``) and S_out must be passed in: neither this
     wrapper nor the library allocates anything.  The library's scratch is a
-    32 MiB static device array shared by all calls, so calls that overlap on
+    96 MiB static device array shared by all calls, so calls that overlap on
     the GPU race; larger problems raise GdnError(GDN_ERR_NOMEM)."""
     lib = _lib.load()
     T, h_k, d_k = k.shape

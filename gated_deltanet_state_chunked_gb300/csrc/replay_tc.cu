@@ -814,9 +814,9 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
 namespace gdn {
 namespace {
 
-// 32 MiB on every GPU that loads the library, held until process exit.  Enough for the
-// records of one 3277-token tail at 32 v-heads ((52 + 1) chunks x 32 heads x 17408 B).
-constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+// 96 MiB on every GPU that loads the library, held until process exit.  Enough for the
+// records of one 3277-token tail at 32 v-heads ((52 + 1) chunks x 32 heads x 41984 B = 67.9 MiB).
+constexpr size_t kStaticScratchBytes = size_t(96) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // Device address of g_static_scratch, resolved once per device with that device current
@@ -855,8 +855,8 @@ extern "C" int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const voi
     const size_t need = replay_tc_workspace_bytes(p.n_seqs, p.total_tokens, p.h_v);
     if (need > kStaticScratchBytes)
       return report_error(GDN_ERR_NOMEM,
-                          "gdn_replay_noalloc: the problem needs more scratch than the 32 MiB static array "
-                          "((ceil(total_tokens/64) + n_seqs) * h_v * 17408 bytes); use gdn_replay");
+                          "gdn_replay_noalloc: the problem needs more scratch than the 96 MiB static array "
+                          "((ceil(total_tokens/64) + n_seqs) * h_v * 41984 bytes); use gdn_replay");
     void* ws = nullptr;
     rc = static_scratch_address(&ws);
     if (rc) return rc;

@@ -107,11 +107,11 @@ int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v
  * (for its cache) and forbids allocations afterwards, or a caller whose
  * process-wide policy routes every device allocation through its own
  * allocator.  gdn_replay takes its scratch from a pool that can grow; this
- * variant instead uses one static device array of 32 MiB that every GPU that
+ * variant instead uses one static device array of 96 MiB that every GPU that
  * loads the library holds until the process exits.
  *   Arguments, layouts, results and error codes are those of gdn_replay.
  *   Limit: the tensor-core path needs (ceil(total_tokens / 64) + n_seqs) * h_v
- *   * 17408 bytes of scratch (a 3277-token tail at 32 v-heads needs 29.5 MB);
+ *   * 41984 bytes of scratch (a 3277-token tail at 32 v-heads needs 67.9 MiB);
  *   a larger problem is rejected with GDN_ERR_NOMEM before anything is
  *   launched.  fp32 inputs and GDN_PRECISE need no scratch.
  *   The first call on a device resolves the static array's device address

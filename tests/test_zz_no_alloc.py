@@ -46,6 +46,13 @@ def test_matches_gdn_replay_on_two_calls_in_a_row():
         assert rel_err(host(O), host(O_ref)) <= TOL_BF16
 
 
+def test_single_layer_3277_token_tail_fits():
+    x = synthetic.workload_inputs("layer_r3277")
+    (O, S), (O_ref, S_ref) = _both(x)
+    assert rel_err(host(S), host(S_ref)) <= TOL_BF16
+    assert rel_err(host(O), host(O_ref)) <= TOL_BF16
+
+
 def test_rejects_a_problem_beyond_the_static_scratch():
     x = synthetic.make_replay_inputs([8192], 16, 32, 128, 128, dtype="bf16", seed=503)
     d = to_device(x)
