@@ -79,66 +79,72 @@ struct PrepParams {
 };
 
 // M = (I + A)^{-1} for a 64x64 strictly lower A (stride MST), by one 128-thread warpgroup
-// (t = thread index in the group, bid = its named barrier).  A's strictly upper blocks are
-// used as scratch.  Diagonal 16x16 blocks by substitution; then At_ik = M_ii A_ik and
-// M_ij = -sum_{k=j}^{i-1} At_ik M_kj along the block diagonals.
+// (t = thread index in the group, bid = its named barrier).  In 32x32 blocks,
+//   M11 = (I + A11)^{-1}, M22 = (I + A22)^{-1}, M21 = -M22 A21 M11, M12 = 0:
+// the diagonal blocks by forward substitution with one column per thread held in registers
+// (each row of A is a broadcast load), then the two products with 8 outputs per thread.  A's
+// upper-right block (zero, unused afterwards) holds A21 M11 in between.
 __device__ void invert_unit_lower(float* A, float* M, int t, int bid) {
   if (t < 64) {
-    const int b = t >> 4, j = t & 15;
-    const float* Ab = A + (16 * b) * MST + 16 * b;
-    float m[16];
+    const int b = t >> 5, j = t & 31;
+    const float* Ab = A + (32 * b) * MST + 32 * b;
+    float m[32];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float a0 = (r == j) ? 1.f : 0.f, a1 = 0.f;
+    for (int r = 0; r < 32; ++r) {
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int s = 0; s < r; s += 2) {
-        a0 = fmaf(-Ab[r * MST + s], m[s], a0);
-        if (s + 1 < r) a1 = fmaf(-Ab[r * MST + s + 1], m[s + 1], a1);
+      for (int s = 0; s + 3 < r; s += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(Ab + r * MST + s);
+        a0 = fmaf(a.x, m[s], a0);
+        a1 = fmaf(a.y, m[s + 1], a1);
+        a2 = fmaf(a.z, m[s + 2], a2);
+        a3 = fmaf(a.w, m[s + 3], a3);
       }
-      m[r] = a0 + a1;
+#pragma unroll
+      for (int s = r & ~3; s < r; ++s) a0 = fmaf(Ab[r * MST + s], m[s], a0);
+      const float x = -((a0 + a1) + (a2 + a3));
+      m[r] = r == j ? 1.f : (r < j ? 0.f : x);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) M[(16 * b + r) * MST + 16 * b + j] = m[r];
+    for (int r = 0; r < 32; ++r) M[(32 * b + r) * MST + 32 * b + j] = m[r];
   } else {
-    for (int i = t - 64; i < 64 * 16; i += 64) {  // zero the strictly upper blocks, 4 at a time
-      const int r = i >> 4, c4 = (i & 15) * 4;
-      if ((c4 >> 4) > (r >> 4)) *reinterpret_cast<float4*>(M + r * MST + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int i = t - 64; i < 256; i += 64)  // M12 = 0
+      *reinterpret_cast<float4*>(M + (i >> 3) * MST + 32 + (i & 7) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   group_sync(bid);
-  for (int task = t; task < 384; task += 128) {
-    const int blk = task >> 6, r = (task >> 2) & 15, cq = (task & 3) * 4;
-    const int i = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
-    const int k = blk < 1 ? 0 : (blk < 3 ? blk - 1 : blk - 3);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int r = t >> 2, c8 = (t & 3) * 8;  // output rows r of a 32x32 block, columns [c8, c8 + 8)
+  {  // X = A21 M11 -> A[0:32][32:64]
+    float x[8];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float m = M[(16 * i + r) * MST + 16 * i + u];
-      const float4 a = *reinterpret_cast<const float4*>(A + (16 * i + u) * MST + 16 * k + cq);
-      acc.x = fmaf(m, a.x, acc.x); acc.y = fmaf(m, a.y, acc.y);
-      acc.z = fmaf(m, a.z, acc.z); acc.w = fmaf(m, a.w, acc.w);
+    for (int i = 0; i < 8; ++i) x[i] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float a = A[(32 + r) * MST + k];
+      const float4 m0 = *reinterpret_cast<const float4*>(M + k * MST + c8);
+      const float4 m1 = *reinterpret_cast<const float4*>(M + k * MST + c8 + 4);
+      x[0] = fmaf(a, m0.x, x[0]); x[1] = fmaf(a, m0.y, x[1]); x[2] = fmaf(a, m0.z, x[2]); x[3] = fmaf(a, m0.w, x[3]);
+      x[4] = fmaf(a, m1.x, x[4]); x[5] = fmaf(a, m1.y, x[5]); x[6] = fmaf(a, m1.z, x[6]); x[7] = fmaf(a, m1.w, x[7]);
     }
-    *reinterpret_cast<float4*>(A + (16 * k + r) * MST + 16 * i + cq) = acc;
+    *reinterpret_cast<float4*>(A + r * MST + 32 + c8) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(A + r * MST + 32 + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
   }
   group_sync(bid);
+  {  // M21 = -M22 X
+    float y[8];
 #pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    for (int task = t; task < (4 - d) * 64; task += 128) {
-      const int i = d + (task >> 6), j = i - d, r = (task >> 2) & 15, cq = (task & 3) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = j; k < i; ++k) {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float a = A[(16 * k + r) * MST + 16 * i + u];
-          const float4 m = *reinterpret_cast<const float4*>(M + (16 * k + u) * MST + 16 * j + cq);
-          acc.x = fmaf(a, m.x, acc.x); acc.y = fmaf(a, m.y, acc.y);
-          acc.z = fmaf(a, m.z, acc.z); acc.w = fmaf(a, m.w, acc.w);
-        }
-      }
-      *reinterpret_cast<float4*>(M + (16 * i + r) * MST + 16 * j + cq) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    for (int i = 0; i < 8; ++i) y[i] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float mm = M[(32 + r) * MST + 32 + k];
+      const float4 x0 = *reinterpret_cast<const float4*>(A + k * MST + 32 + c8);
+      const float4 x1 = *reinterpret_cast<const float4*>(A + k * MST + 32 + c8 + 4);
+      y[0] = fmaf(mm, x0.x, y[0]); y[1] = fmaf(mm, x0.y, y[1]); y[2] = fmaf(mm, x0.z, y[2]); y[3] = fmaf(mm, x0.w, y[3]);
+      y[4] = fmaf(mm, x1.x, y[4]); y[5] = fmaf(mm, x1.y, y[5]); y[6] = fmaf(mm, x1.z, y[6]); y[7] = fmaf(mm, x1.w, y[7]);
     }
-    group_sync(bid);
+    *reinterpret_cast<float4*>(M + (32 + r) * MST + c8) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+    *reinterpret_cast<float4*>(M + (32 + r) * MST + c8 + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
   }
+  group_sync(bid);
 }
 
 // Row sum of squares of a 64-element bf16 row held as 8 16-byte chunks (any order).
