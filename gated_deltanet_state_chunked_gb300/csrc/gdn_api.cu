@@ -221,8 +221,20 @@ int gdn_chunk_operator(const gdn_dims* dims, const void* k, const float* g, cons
   p.h_k = dims->h_k; p.h_v = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
   p.augmented = 1; p.l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
   p.write_O = 0; p.scale = 1.f; p.status = status;
-  cudaError_t e = launch_replay_simt(p, dims->dtype == GDN_BF16, static_cast<cudaStream_t>(stream));
+  // Two passes: the chunk-shared quantities once per (chunk, v-head) into pool scratch, then the
+  // row slices of the augmented state [S; P] read them.
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = simt_records_bytes(p.n_seqs, p.total_tokens, p.h_v);
+  cudaMemPool_t pool = nullptr;
+  int prc = scratch_pool(&pool);
+  if (prc) return prc;
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+  if (e != cudaSuccess) return fail(GDN_ERR_NOMEM, "scratch of %zu bytes: %s", bytes, cudaGetErrorString(e));
+  e = launch_replay_simt_two_pass(p, dims->dtype == GDN_BF16, ws, bytes, st);
+  const cudaError_t ef = cudaFreeAsync(ws, st);
   if (e != cudaSuccess) return cuda_fail(e, "gdn_chunk_operator launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch release");
   return GDN_OK;
 }
 

@@ -29,9 +29,15 @@ struct SimtParams {
   int write_O;
   float scale;
   int* status;    // sticky device status word
+  unsigned char* rec;  // optional per-(chunk, v-head) records of the chunk-shared quantities (scratch)
 };
 
 cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t stream);
+// Scratch bytes of the two-kernel CUDA-core path (chunk-parallel prep, then the row-slice scan).
+size_t simt_records_bytes(int n_seqs, int total_tokens, int h_v);
+// The same computation as launch_replay_simt, with the chunk-shared work (norms, gates, Gram,
+// (I + A)^{-1}) done once per (chunk, v-head) by a prep kernel into `workspace` first.
+cudaError_t launch_replay_simt_two_pass(SimtParams p, int bf16, void* workspace, size_t bytes, cudaStream_t stream);
 
 // Tensor-core path (bf16 inputs, d_k = d_v = 128, total_tokens > 0): a chunk-parallel
 // prep kernel writes per-(chunk, v-head) records into `workspace`, then the scan

@@ -28,13 +28,14 @@
 #include <cuda_bf16.h>
 
 #include "gdn_internal.cuh"
+#include "tc_common.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int C = kChunk;
 constexpr int RS = 32;                // state rows per CTA
-constexpr int KST = kMaxHead + 4;     // row stride of K/Q/S tiles (floats)
+constexpr int KST = kMaxHead + 1;     // row stride of K/Q/S tiles (floats): column reads across rows hit distinct banks
 constexpr int VST = RS + 1;           // row stride of V/R/U tiles
 constexpr int GST = C + 1;            // row stride of the 64x64 tiles
 constexpr int NT = 256;
@@ -52,12 +53,154 @@ struct Smem {
   float gam[C];        // exp(G_t)
   float wend[C];       // exp(G_last - G_t)
   float beta[C];
+  int scratch[20];
 };
 
 __device__ __forceinline__ float ld_in(const float* p, size_t i) { return p[i]; }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
 __device__ __forceinline__ void st_out(float* p, size_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------------------------
+// Two-pass mode: the chunk-shared quantities, once per (chunk, v-head).  Record (fp32):
+//   M = (I + A)^{-1} [64][64], P [64][64] (zero without outputs), gamma_t, exp(G_last - G_t),
+//   beta_t, rk_t (key norm factor), rq_t (query norm factor times scale).
+constexpr int REC_M = 0, REC_P = 4096, REC_GAM = 8192, REC_WEND = 8256, REC_BETA = 8320, REC_RK = 8384,
+              REC_RQ = 8448, REC_FLOATS = 8512;
+
+struct PrepSmem {
+  float K[C * KST];
+  float Q[C * KST];
+  float A[C * tcp::MST];
+  float M[C * tcp::MST];
+  float G[C], beta[C], rk[C], rq[C];
+  int scratch[20];
+};
+
+// One CTA per (global chunk, v-head): load and normalise the chunk's keys (and queries), gate
+// sums, the gated Gram matrices A and P, and M = (I + A)^{-1}; write the record.
+template <typename Tin>
+__global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int gc = blockIdx.x, h = blockIdx.y;
+  const int DK = p.d_k;
+  int t0, n;
+  if (p.cu) {
+    const tcp::ChunkInfo ci = tcp::chunk_info(p.cu, p.n_seqs, p.total_tokens, -1, gc, sm.scratch);
+    if (gc >= ci.total || ci.gc_seq < 0) return;
+    t0 = p.cu[ci.gc_seq] + ci.gc_idx * C;
+    n = min(C, p.cu[ci.gc_seq + 1] - t0);
+  } else {
+    if (gc >= tcp::chunks_of(p.total_tokens)) return;
+    t0 = gc * C;
+    n = min(C, p.total_tokens - t0);
+  }
+  const int hk = h / (p.h_v / p.h_k);
+  const Tin* __restrict__ q = static_cast<const Tin*>(p.q);
+  const Tin* __restrict__ k = static_cast<const Tin*>(p.k);
+  float* rec = reinterpret_cast<float*>(p.rec) + ((size_t)gc * p.h_v + h) * REC_FLOATS;
+
+#pragma unroll 8
+  for (int i = tid; i < C * DK; i += NT) {
+    const int t = i / DK, d = i % DK;
+    const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d;
+    sm.K[t * KST + d] = t < n ? ld_in(k, off) : 0.f;
+    if (p.write_O) sm.Q[t * KST + d] = t < n ? ld_in(q, off) : 0.f;
+  }
+  if (tid < C) {
+    const bool in = tid < n;
+    sm.G[tid] = in ? p.g[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
+    sm.beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
+  }
+  __syncthreads();
+  // per-token L2 normalisation (q also takes the scale), gate prefix sums
+  for (int t = warp; t < C; t += NT / 32) {
+    float sk = 0.f, sq = 0.f;
+    for (int d = lane; d < DK; d += 32) {
+      const float a = sm.K[t * KST + d];
+      sk += a * a;
+      if (p.write_O) { const float b = sm.Q[t * KST + d]; sq += b * b; }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    }
+    const float fk = p.l2norm ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
+    const float fq = (p.l2norm ? 1.f / sqrtf(sq + 1e-6f) : 1.f) * p.scale;
+    for (int d = lane; d < DK; d += 32) {
+      sm.K[t * KST + d] *= fk;
+      if (p.write_O) sm.Q[t * KST + d] *= fq;
+    }
+    if (lane == 0) {
+      sm.rk[t] = fk;
+      sm.rq[t] = fq;
+    }
+  }
+  if (warp == 0) {
+    float a = sm.G[lane], b = sm.G[lane + 32];
+    for (int o = 1; o < 32; o <<= 1) {
+      const float xa = __shfl_up_sync(0xffffffffu, a, o);
+      const float xb = __shfl_up_sync(0xffffffffu, b, o);
+      if (lane >= o) { a += xa; b += xb; }
+    }
+    b += __shfl_sync(0xffffffffu, a, 31);
+    sm.G[lane] = a;
+    sm.G[lane + 32] = b;
+  }
+  __syncthreads();
+  {  // Gram matrices: A (strictly lower, gated, beta-weighted) into shared memory, P into the record
+    const int ti = (tid / 16) * 4, si = (tid % 16) * 4;
+    float akk[4][4] = {}, aqk[4][4] = {};
+    for (int d = 0; d < DK; ++d) {
+      float a[4], b[4], c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = sm.K[(ti + i) * KST + d];
+        b[i] = sm.K[(si + i) * KST + d];
+        c[i] = p.write_O ? sm.Q[(ti + i) * KST + d] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          akk[i][j] = fmaf(a[i], b[j], akk[i][j]);
+          aqk[i][j] = fmaf(c[i], b[j], aqk[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = ti + i;
+      float pv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int s = si + j;
+        const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
+        sm.A[t * tcp::MST + s] = s < t ? sm.beta[t] * decay * akk[i][j] : 0.f;
+        pv[j] = s <= t ? decay * aqk[i][j] : 0.f;
+      }
+      *reinterpret_cast<float4*>(rec + REC_P + t * C + si) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+    }
+  }
+  __syncthreads();
+  if (warp < 4) {
+    tcp::invert_unit_lower(sm.A, sm.M, tid, 1);
+  } else if (tid - 128 < C) {
+    const int t = tid - 128;
+    const float Gl = sm.G[C - 1];
+    rec[REC_GAM + t] = expf(sm.G[t]);
+    rec[REC_WEND + t] = expf(Gl - sm.G[t]);
+    rec[REC_BETA + t] = sm.beta[t];
+    rec[REC_RK + t] = sm.rk[t];
+    rec[REC_RQ + t] = sm.rq[t];
+  }
+  __syncthreads();
+  for (int i = tid; i < C * C / 4; i += NT) {
+    const int t = i / (C / 4), s4 = (i % (C / 4)) * 4;
+    *reinterpret_cast<float4*>(rec + REC_M + t * C + s4) = *reinterpret_cast<const float4*>(sm.M + t * tcp::MST + s4);
+  }
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
@@ -81,6 +224,10 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     return;
   }
 
+  // two-pass mode: global index of this sequence's first chunk in the records
+  int first = 0;
+  if (p.rec && p.cu) first = tcp::chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, sm.scratch).first;
+
   // entering state of this slice
   for (int i = tid; i < RS * DK; i += NT) {
     const int r = i / DK, d = i % DK, rg = row0 + r;
@@ -93,9 +240,57 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     sm.S[r * KST + d] = s;
   }
 
-  for (int t0 = t_begin; t0 < t_end; t0 += C) {
+  for (int t0 = t_begin, ck = 0; t0 < t_end; t0 += C, ++ck) {
     const int n = min(C, t_end - t0);
     __syncthreads();
+    if (p.rec) {
+      // ---- chunk-shared quantities from the record; keys (and queries) scaled by their norms
+      const float* R = reinterpret_cast<const float*>(p.rec) + ((size_t)(first + ck) * p.h_v + h) * REC_FLOATS;
+#pragma unroll 8
+      for (int i = tid; i < C * DK; i += NT) {
+        const int t = i / DK, d = i % DK;
+        const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d;
+        sm.K[t * KST + d] = t < n ? R[REC_RK + t] * ld_in(k, off) : 0.f;
+        if (p.write_O) sm.Q[t * KST + d] = t < n ? R[REC_RQ + t] * ld_in(q, off) : 0.f;
+      }
+      for (int i = tid; i < C * RS; i += NT) {
+        const int t = i / RS, r = i % RS, rg = row0 + r;
+        float x = 0.f;
+        if (t < n && rg < DV) x = ld_in(v, ((size_t)(t0 + t) * p.h_v + h) * DV + rg);
+        sm.V[t * VST + r] = x;
+      }
+#pragma unroll 8
+      for (int i = tid; i < C * C; i += NT) {
+        const int t = i / C, s2 = i % C;
+        sm.M[t * GST + s2] = R[REC_M + i];
+        if (p.write_O) sm.P[t * GST + s2] = R[REC_P + i];
+      }
+      if (tid < C) {
+        sm.gam[tid] = R[REC_GAM + tid];
+        sm.wend[tid] = R[REC_WEND + tid];
+        sm.beta[tid] = R[REC_BETA + tid];
+      }
+      __syncthreads();
+      {  // X = K S0^T: this thread's chunk rows t0x .. t0x + 3, slice rows rx, rx + 1
+        const int rx = (tid % 16) * 2, t0x = (tid / 16) * 4;
+        float x[4][2] = {};
+        for (int d = 0; d < DK; ++d) {
+          const float s0 = sm.S[rx * KST + d], s1 = sm.S[(rx + 1) * KST + d];
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const float kv = sm.K[(t0x + a) * KST + d];
+            x[a][0] = fmaf(kv, s0, x[a][0]);
+            x[a][1] = fmaf(kv, s1, x[a][1]);
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          sm.X[(t0x + a) * VST + rx] = x[a][0];
+          sm.X[(t0x + a) * VST + rx + 1] = x[a][1];
+        }
+      }
+      __syncthreads();
+    } else {
     // ---- load the chunk
     for (int i = tid; i < C * DK; i += NT) {
       const int t = i / DK, d = i % DK;
@@ -217,6 +412,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
       }
     }
     __syncthreads();
+    }
 
     // ---- R = diag(beta) (V - diag(gamma) X)   (in place in V)
     for (int i = tid; i < C * RS; i += NT) {
@@ -249,26 +445,23 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
         st_out(O, ((size_t)(t0 + t) * p.h_v + h) * DV + rg, acc);
       }
     }
-    constexpr int PER = RS * kMaxHead / NT;  // 16 state entries per thread
+    constexpr int PER = RS * kMaxHead / NT;  // 16 state entries per thread: rows r0 + 2 e, column d
+    const int sd = tid % kMaxHead, r0 = tid / kMaxHead;
     float snew[PER];
-    const float gC = sm.gam[C - 1];
+    if (sd < DK) {
+      const float gC = sm.gam[C - 1];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      const int i = tid + e * NT;
-      const int r = i / kMaxHead, d = i % kMaxHead;
-      float acc = 0.f;
-      if (d < DK) {
-        acc = gC * sm.S[r * KST + d];
-        for (int t = 0; t < C; ++t) acc = fmaf(sm.wend[t] * sm.V[t * VST + r], sm.K[t * KST + d], acc);
+      for (int e = 0; e < PER; ++e) snew[e] = gC * sm.S[(r0 + 2 * e) * KST + sd];
+      for (int t = 0; t < C; ++t) {
+        const float wk = sm.wend[t] * sm.K[t * KST + sd];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) snew[e] = fmaf(sm.V[t * VST + r0 + 2 * e], wk, snew[e]);
       }
-      snew[e] = acc;
     }
     __syncthreads();
+    if (sd < DK) {
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      const int i = tid + e * NT;
-      const int r = i / kMaxHead, d = i % kMaxHead;
-      if (d < DK) sm.S[r * KST + d] = snew[e];
+      for (int e = 0; e < PER; ++e) sm.S[(r0 + 2 * e) * KST + sd] = snew[e];
     }
   }
   __syncthreads();
@@ -304,6 +497,36 @@ cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t strea
     simt_chunk_scan_kernel<float><<<grid, NT, smem, stream>>>(p);
   }
   return cudaGetLastError();
+}
+
+size_t simt_records_bytes(int n_seqs, int total_tokens, int h_v) {
+  const size_t chunks = (size_t)tcp::chunks_of(total_tokens) + (size_t)n_seqs;  // >= sum of ceil(len / 64)
+  return chunks * (size_t)h_v * REC_FLOATS * sizeof(float);
+}
+
+cudaError_t launch_replay_simt_two_pass(SimtParams p, int bf16, void* workspace, size_t bytes, cudaStream_t stream) {
+  if (p.n_seqs == 0) return cudaSuccess;
+  if (!workspace || bytes < simt_records_bytes(p.n_seqs, p.total_tokens, p.h_v)) return cudaErrorInvalidValue;
+  p.rec = static_cast<unsigned char*>(workspace);
+  const int chunks_ub = tcp::chunks_of(p.total_tokens) + (p.cu ? p.n_seqs : 0);
+  if (p.total_tokens > 0) {
+    const dim3 grid(chunks_ub, p.h_v);
+    const size_t smem = sizeof(PrepSmem);
+    cudaError_t e;
+    if (bf16) {
+      e = cudaFuncSetAttribute(simt_chunk_prep_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+      if (e != cudaSuccess) return e;
+      simt_chunk_prep_kernel<__nv_bfloat16><<<grid, NT, smem, stream>>>(p);
+    } else {
+      e = cudaFuncSetAttribute(simt_chunk_prep_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      simt_chunk_prep_kernel<float><<<grid, NT, smem, stream>>>(p);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return launch_replay_simt(p, bf16, stream);
 }
 
 }  // namespace gdn

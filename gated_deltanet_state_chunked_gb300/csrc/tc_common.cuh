@@ -107,5 +107,79 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
   return r;
 }
 
+// Named barrier over one 128-thread warpgroup (ids 1, 2, ...; 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+constexpr int MST = 68;  // row stride (floats) of the 64x64 fp32 work matrices (16-byte aligned rows)
+
+// M = (I + A)^{-1} for a 64x64 strictly lower A (stride MST), by one 128-thread warpgroup
+// (t = thread index in the group, bid = its named barrier).  In 32x32 blocks,
+//   M11 = (I + A11)^{-1}, M22 = (I + A22)^{-1}, M21 = -M22 A21 M11, M12 = 0:
+// the diagonal blocks by forward substitution with one column per thread held in registers
+// (each row of A is a broadcast load), then the two products with 8 outputs per thread.  A's
+// upper-right block (zero, unused afterwards) holds A21 M11 in between.
+__device__ inline void invert_unit_lower(float* A, float* M, int t, int bid) {
+  if (t < 64) {
+    const int b = t >> 5, j = t & 31;
+    const float* Ab = A + (32 * b) * MST + 32 * b;
+    float m[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int s = 0; s + 3 < r; s += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(Ab + r * MST + s);
+        a0 = fmaf(a.x, m[s], a0);
+        a1 = fmaf(a.y, m[s + 1], a1);
+        a2 = fmaf(a.z, m[s + 2], a2);
+        a3 = fmaf(a.w, m[s + 3], a3);
+      }
+#pragma unroll
+      for (int s = r & ~3; s < r; ++s) a0 = fmaf(Ab[r * MST + s], m[s], a0);
+      const float x = -((a0 + a1) + (a2 + a3));
+      m[r] = r == j ? 1.f : (r < j ? 0.f : x);
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) M[(32 * b + r) * MST + 32 * b + j] = m[r];
+  } else {
+    for (int i = t - 64; i < 256; i += 64)  // M12 = 0
+      *reinterpret_cast<float4*>(M + (i >> 3) * MST + 32 + (i & 7) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  group_sync(bid);
+  const int r = t >> 2, c8 = (t & 3) * 8;  // output rows r of a 32x32 block, columns [c8, c8 + 8)
+  {  // X = A21 M11 -> A[0:32][32:64]
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float a = A[(32 + r) * MST + k];
+      const float4 m0 = *reinterpret_cast<const float4*>(M + k * MST + c8);
+      const float4 m1 = *reinterpret_cast<const float4*>(M + k * MST + c8 + 4);
+      x[0] = fmaf(a, m0.x, x[0]); x[1] = fmaf(a, m0.y, x[1]); x[2] = fmaf(a, m0.z, x[2]); x[3] = fmaf(a, m0.w, x[3]);
+      x[4] = fmaf(a, m1.x, x[4]); x[5] = fmaf(a, m1.y, x[5]); x[6] = fmaf(a, m1.z, x[6]); x[7] = fmaf(a, m1.w, x[7]);
+    }
+    *reinterpret_cast<float4*>(A + r * MST + 32 + c8) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(A + r * MST + 32 + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+  }
+  group_sync(bid);
+  {  // M21 = -M22 X
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float mm = M[(32 + r) * MST + 32 + k];
+      const float4 x0 = *reinterpret_cast<const float4*>(A + k * MST + 32 + c8);
+      const float4 x1 = *reinterpret_cast<const float4*>(A + k * MST + 32 + c8 + 4);
+      y[0] = fmaf(mm, x0.x, y[0]); y[1] = fmaf(mm, x0.y, y[1]); y[2] = fmaf(mm, x0.z, y[2]); y[3] = fmaf(mm, x0.w, y[3]);
+      y[4] = fmaf(mm, x1.x, y[4]); y[5] = fmaf(mm, x1.y, y[5]); y[6] = fmaf(mm, x1.z, y[6]); y[7] = fmaf(mm, x1.w, y[7]);
+    }
+    *reinterpret_cast<float4*>(M + (32 + r) * MST + c8) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+    *reinterpret_cast<float4*>(M + (32 + r) * MST + c8 + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+  }
+  group_sync(bid);
+}
+
 }  // namespace tcp
 }  // namespace gdn

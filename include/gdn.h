@@ -139,7 +139,10 @@ int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const void* k, const
  *               S_out = S_in T_C^T + S_local in this ABI's state layout
  *   Slocal_out  fp32 [n_seqs][h_v][d_v][d_k]
  * q is not needed; dims->scale and GDN_STATE_ONLY are ignored.  Computed in
- * fp32 on CUDA cores whatever the input dtype.
+ * fp32 on CUDA cores whatever the input dtype, in two passes: the chunk-shared
+ * quantities ((I + A)^{-1}, gates, norms) once per (64-token piece, v-head)
+ * into pool scratch of (ceil(total_tokens / 64) + n_seqs) * h_v * 34048 bytes,
+ * then the row slices of the augmented state.
  */
 int gdn_chunk_operator(const gdn_dims* dims, const void* k, const float* g, const float* beta, const void* v,
                        const int32_t* cu_seqlens, float* T_out, float* Slocal_out, void* stream);
