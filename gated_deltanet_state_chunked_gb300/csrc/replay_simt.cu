@@ -246,6 +246,64 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     if (p.rec) {
       // ---- chunk-shared quantities from the record; keys (and queries) scaled by their norms
       const float* R = reinterpret_cast<const float*>(p.rec) + ((size_t)(first + ck) * p.h_v + h) * REC_FLOATS;
+      bool vec = false;
+      if constexpr (sizeof(Tin) == 4) vec = (DK == kMaxHead) && (DV % RS == 0);
+      if (vec) {
+        // fp32, 128-dim heads: every global load of the chunk issued before the first shared store
+        const float* kf = reinterpret_cast<const float*>(k);
+        const float* qf = reinterpret_cast<const float*>(q);
+        const float* vf = reinterpret_cast<const float*>(v);
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 kv[8], qv[8], mv[4], pv[4], vv[2];
+        float rkv[8], rqv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+          const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d4;
+          kv[j] = t < n ? *reinterpret_cast<const float4*>(kf + off) : z4;
+          qv[j] = (t < n && p.write_O) ? *reinterpret_cast<const float4*>(qf + off) : z4;
+          rkv[j] = R[REC_RK + t];
+          rqv[j] = R[REC_RQ + t];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mv[j] = *reinterpret_cast<const float4*>(R + REC_M + (tid + j * NT) * 4);
+          pv[j] = p.write_O ? *reinterpret_cast<const float4*>(R + REC_P + (tid + j * NT) * 4) : z4;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int i4 = tid + j * NT, t = i4 >> 3, r4 = (i4 & 7) * 4;
+          vv[j] = (t < n && row0 + r4 < DV)
+                      ? *reinterpret_cast<const float4*>(vf + ((size_t)(t0 + t) * p.h_v + h) * DV + row0 + r4)
+                      : z4;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+          float* kd = sm.K + t * KST + d4;
+          kd[0] = rkv[j] * kv[j].x; kd[1] = rkv[j] * kv[j].y; kd[2] = rkv[j] * kv[j].z; kd[3] = rkv[j] * kv[j].w;
+          if (p.write_O) {
+            float* qd = sm.Q + t * KST + d4;
+            qd[0] = rqv[j] * qv[j].x; qd[1] = rqv[j] * qv[j].y; qd[2] = rqv[j] * qv[j].z; qd[3] = rqv[j] * qv[j].w;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = (tid + j * NT) * 4, t = i / C, s2 = i % C;
+          float* md = sm.M + t * GST + s2;
+          md[0] = mv[j].x; md[1] = mv[j].y; md[2] = mv[j].z; md[3] = mv[j].w;
+          if (p.write_O) {
+            float* pd = sm.P + t * GST + s2;
+            pd[0] = pv[j].x; pd[1] = pv[j].y; pd[2] = pv[j].z; pd[3] = pv[j].w;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int i4 = tid + j * NT, t = i4 >> 3, r4 = (i4 & 7) * 4;
+          float* vd = sm.V + t * VST + r4;
+          vd[0] = vv[j].x; vd[1] = vv[j].y; vd[2] = vv[j].z; vd[3] = vv[j].w;
+        }
+      } else {
 #pragma unroll 8
       for (int i = tid; i < C * DK; i += NT) {
         const int t = i / DK, d = i % DK;
@@ -264,6 +322,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
         const int t = i / C, s2 = i % C;
         sm.M[t * GST + s2] = R[REC_M + i];
         if (p.write_O) sm.P[t * GST + s2] = R[REC_P + i];
+      }
       }
       if (tid < C) {
         sm.gam[tid] = R[REC_GAM + tid];
