@@ -67,17 +67,19 @@ __global__ void __launch_bounds__(NT) compose_simt_kernel(ComposeParams p) {
 // ---------------------------------------------------------------------------------------------
 // d_k = d_v = 128: register-tiled kernel.  One CTA owns 32 rows of one head's state (kept in
 // shared memory) and walks the K steps.  T_j (64 KB, contiguous) and S_local_j's 32-row slice
-// arrive by bulk copies two steps ahead of use.  Thread (b, g) computes rows 4 b .. 4 b + 3 and
-// columns g + 16 i (i < 8) of S T_j^T with float4 shared loads (each loaded T value feeds four
-// rows, each S value eight columns), walking k in an order rotated by 4 g so that the eight
-// threads of a quarter warp read eight different 16-byte chunks of their T and S rows.
-constexpr int CR = 32, CNT = 128, CPAD = 132, CD = 128;
+// arrive by bulk copies two steps ahead of use.  Thread (b, g) of each 128-thread half computes
+// rows 4 b .. 4 b + 3 and columns g + 16 i (i < 8) of S T_j^T over its half of k with float4
+// shared loads (each loaded T value feeds four rows, each S value eight columns), walking k in an
+// order rotated by 4 g so that the eight threads of a quarter warp read eight different 16-byte
+// chunks of their T and S rows; the second half's partial sums are added through shared memory.
+constexpr int CR = 32, CNT = 256, CPAD = 132, CD = 128;
 struct CLay {
   static constexpr uint32_t TB = 0;                       // 2 x T_j [128][128] fp32
   static constexpr uint32_t TBYTES = CD * CD * 4;         // 65536
   static constexpr uint32_t SS = 2 * TBYTES;              // S slice [32][132]
   static constexpr uint32_t LB = SS + CR * CPAD * 4;      // 2 x S_local slice [32][128]
-  static constexpr uint32_t BARS = LB + 2 * CR * CD * 4;  // bar_t[2], bar_l[2], abort flag
+  static constexpr uint32_t RED = LB + 2 * CR * CD * 4;   // partial sums of the second k half [32][128]
+  static constexpr uint32_t BARS = RED + CR * CD * 4;     // bar_t[2], bar_l[2], abort flag
   static constexpr uint32_t TOTAL = BARS + 64;
 };
 
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(CNT, 1) compose_tiled_kernel(ComposeParams p) 
   uint64_t* bar_t = reinterpret_cast<uint64_t*>(cmem + L::BARS);
   uint64_t* bar_l = bar_t + 2;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cmem + L::BARS + 32);
-  const int tid = threadIdx.x, lane = tid & 31, rb = 4 * (tid >> 4), g = tid & 15;
+  const int tid = threadIdx.x, lane = tid & 31, kh = tid >> 7, rb = 4 * ((tid & 127) >> 4), g = tid & 15;
+  float* Red = reinterpret_cast<float*>(cmem + L::RED);
   const int h = blockIdx.y, row0 = blockIdx.x * CR;
   const size_t sbase = (size_t)h * CD * CD;
 
@@ -144,8 +147,8 @@ __global__ void __launch_bounds__(CNT, 1) compose_tiled_kernel(ComposeParams p) 
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[a][i] = 0.f;
 #pragma unroll 2
-    for (int q = 0; q < CD / 4; ++q) {
-      const int kk = ((q + g) & (CD / 4 - 1)) * 4;
+    for (int q = 0; q < CD / 8; ++q) {
+      const int kk = (kh * (CD / 8) + ((q + g) & (CD / 8 - 1))) * 4;
       float4 s4[4], t4[8];
 #pragma unroll
       for (int a = 0; a < 4; ++a) s4[a] = *reinterpret_cast<const float4*>(Sx + (rb + a) * CPAD + kk);
@@ -161,15 +164,25 @@ __global__ void __launch_bounds__(CNT, 1) compose_tiled_kernel(ComposeParams p) 
           acc[a][i] = fmaf(s4[a].w, t4[i].w, acc[a][i]);
         }
     }
-    __syncthreads();  // every read of the state slice and of T_j is done
+    if (kh == 1) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) Red[(rb + a) * CD + g + 16 * i] = acc[a][i];
+    }
+    __syncthreads();  // every read of the state slice and of T_j is done; partial sums are in place
     if (tid < 32 && j + 2 < p.K) issue_t(j + 2);
     wait(&bar_l[j & 1], par);
     const float* Lb = reinterpret_cast<const float*>(cmem + L::LB + (j & 1) * (CR * CD * 4));
+    if (kh == 0) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        Sx[(rb + a) * CPAD + g + 16 * i] = acc[a][i] + Lb[(rb + a) * CD + g + 16 * i];
+        for (int i = 0; i < 8; ++i) {
+          const int o = (rb + a) * CD + g + 16 * i;
+          Sx[(rb + a) * CPAD + g + 16 * i] = (acc[a][i] + Red[o]) + Lb[o];
+        }
+    }
     __syncthreads();  // the new state slice is complete; S_local_j's buffer is free
     if (tid == 0 && j + 2 < p.K) issue_l(j + 2);
   }
