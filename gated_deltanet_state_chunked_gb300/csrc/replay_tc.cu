@@ -14,17 +14,16 @@
 // Two kernels:
 //  * chunk_prep_kernel -- one CTA per (chunk, key head), all chunks of all tails
 //    in parallel: K K^T on tcgen05, the gated A, and M = (I + A)^{-1} on CUDA
-//    cores (16x16 diagonal blocks by substitution, then block merges), written
+//    cores (32x32 diagonal blocks by forward substitution, then one block merge), written
 //    with beta, G and rk to a per-(chunk, v-head) record in scratch memory.
-//  * chunk_scan_kernel -- one CTA per R-row slice (R = 32 or 64 rows of d_v) of
-//    one (tail, v-head) state, walking the tail's chunks.  Per chunk:
-//      Q K^T              bf16 (exact inputs)                          M=64  N=64
-//      [Mw_hi|Mw_lo][K;K] bf16 hi/lo split of the computed factor        M=64  N=128 K=128
-//      [Mb_hi|Mb_lo][V;V] same                                           M=64  N=R   K=128
-//      W S0^T             tf32 (operands rounded to nearest)             M=64  N=R   K=128
-//      Q [S0_hi|S0_lo]^T  bf16 split of the state                        M=64  N=R   K=256
-//      [K^T|K^T][U^hi;U^lo] bf16 split of the scaled U                   M=128 N=R   K=128
-//      P U                tf32                                           M=64  N=R   K=64
+//  * chunk_scan_kernel -- one CTA per 32-row slice of d_v of one (tail, v-head)
+//    state, walking the tail's chunks.  Per chunk:
+//      K^T Mw^T           bf16 (computed factor rounded once)            M=128 N=64  K=64
+//      [Mb_hi|Mb_lo][V;V] bf16 hi/lo split of the computed factor        M=128 N=32  K=128
+//      [W;Q] S0^T         tf32 (W and S0 rounded to nearest, Q exact)    M=128 N=32  K=128
+//      [K^T|K^T][U^hi;U^lo] bf16 split of the scaled U                   M=128 N=32  K=128
+//      P U                tf32                                           M=128 N=32  K=64
+//    (the M=128 shapes with 64 meaningful rows put them where the epilogue needs them)
 //    all accumulated in fp32 in TMEM; the state slice stays in fp32 registers.
 // Padded tokens past a tail's end get beta = g = 0 (identity transitions).
 #include <cuda.h>
@@ -291,26 +290,28 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 // ---------------------------------------------------------------------------------------------
 template <int R>
 struct ScanLay {
-  static constexpr uint32_t KQ = 0;                 // 2 buffers of bf16 [K;Q]: 2 d_k atoms x (128 rows x 128 B)
-  static constexpr uint32_t VT = KQ + 65536;        // bf16 V atom: 64 tokens x 128 B
+  static constexpr uint32_t KB = 0;                 // 2 buffers of bf16 K: 2 d_k atoms x (64 rows x 128 B)
+  static constexpr uint32_t QB = KB + 32768;        // bf16 Q of the chunk being staged: 2 d_k atoms x (64 rows x 128 B)
+  static constexpr uint32_t VT = QB + 16384;        // bf16 V atom: 64 tokens x 128 B
   static constexpr uint32_t R1 = VT + 8192;         // record part 1: Mb hi|lo (16 KB), Mw (8 KB)
   static constexpr uint32_t R2 = R1 + kRecPart1;    // 2 buffers of record part 2: P (16 KB), factors (1 KB)
-  static constexpr uint32_t WQ = R2 + 2 * 18432;    // fp32 W (64 rows x 4 atoms), tf32-rounded
-  static constexpr uint32_t UH = WQ + 32768;        // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
+  static constexpr uint32_t WQ = R2 + 2 * 18432;    // fp32 [W;Q] (128 rows x 4 atoms): W tf32-rounded, Q exact
+  static constexpr uint32_t UH = WQ + 65536;        // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
   static constexpr uint32_t UT = UH + 16384;        // fp32 U^T (R rows x 2 atoms)
   static constexpr uint32_t S32 = UT + R * 256;     // fp32 state slice (R rows x 4 atoms), tf32-rounded
-  static constexpr uint32_t SH = S32 + R * 512;     // bf16 state: hi (R rows x 2 atoms), then lo
-  static constexpr uint32_t BARS = SH + R * 512;
+  static constexpr uint32_t BARS = S32 + R * 512;
   static constexpr uint32_t TOTAL = BARS + 256;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
-  // TMEM columns
-  static constexpr uint32_t cW = 0, cU = 64, cD1w = 64 + 2 * R, cD1q = 64 + 3 * R, cD2 = 64 + 4 * R,
-                            cPU = 64 + 5 * R;
-  static constexpr uint32_t TMEM_COLS = 256;
-  static_assert(64 + 6 * R <= TMEM_COLS, "TMEM columns");
+  // TMEM columns.  All accumulators use the M=128 layout (lane = row).  [W;Q] S0^T and U~ put
+  // the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127 (Q S0^T; P U is aimed there too).
+  // U~, [W;Q] S0^T and P U have one copy per chunk parity: a chunk's outputs are read back
+  // while the next chunk's MMAs run.
+  static constexpr uint32_t cW = 0, cU = 64, cD1 = 64 + 2 * R, cD2 = 64 + 4 * R, cPU = 64 + 5 * R;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(64 + 7 * R <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
-  static_assert(R2 % 1024 == 0 && WQ % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 && S32 % 1024 == 0 &&
-                    SH % 1024 == 0,
+  static_assert(QB % 1024 == 0 && R2 % 1024 == 0 && WQ % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 &&
+                    S32 % 1024 == 0 && R1 >= 8192,
                 "tile alignment");
 };
 
@@ -336,13 +337,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // Advance a shared-memory descriptor's start address by a byte offset (multiple of 16).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
-// Warp-specialised scan.  Warps 0-3 ("chain") carry the state from chunk to chunk and
-// finish each chunk's outputs while its state update is in flight:
-//   D1w = W S0^T -> U = U~ - D1w, U^ -> D2 = K^T U^ (state), P U (outputs) -> S = gamma_C S + D2.
-// Warps 4-7 ("prep") run one chunk ahead: the W^T and U~ MMAs, the tf32 W tile, Q S0^T once
-// the chain has published the chunk's bf16 state, and all loads.  The groups hand over
-// through mbarriers that complete once per chunk; MMAs are issued by several threads in
-// different warps so that independent instruction streams do not queue behind one issuer.
+// Warp-specialised scan.  Warps 0-3 ("chain") carry the state from chunk to chunk:
+//   D1 = [W;Q] S0^T -> U = U~ - W S0^T, U^ -> D2 = K^T U^ (state), P U (outputs) -> S = gamma_C S + D2.
+// Warps 0-1 form U from the token rows 0-63 of D1 while warps 2-3 write the previous chunk's
+// outputs from rows 64-127 (Q S0^T) and P U, so the output epilogue is off the chunk-to-chunk
+// chain.  Warps 4-7 ("prep") run one chunk ahead: the W^T and U~ MMAs, the fp32 [W;Q] tile
+// and all loads.  The groups hand over through mbarriers that complete once per chunk; MMAs
+// are issued by threads in different warps so that independent streams do not queue behind
+// one issuer.
 template <int R>
 __global__ void __launch_bounds__(NT, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -352,18 +354,16 @@ __global__ void __launch_bounds__(NT, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
-  uint64_t* bar_kq = bars + 0;   // [2] loads of [K;Q]
+  uint64_t* bar_kq = bars + 0;   // [2] loads of K and Q
   uint64_t* bar_r2 = bars + 2;   // [2] loads of record part 2
   uint64_t* bar_r1 = bars + 4;   // V + record part 1
   uint64_t* bar_w = bars + 5;    // MMA W^T
   uint64_t* bar_u = bars + 6;    // MMA U~
-  uint64_t* bar_d1 = bars + 7;   // MMA W S0^T
+  uint64_t* bar_d1 = bars + 7;   // MMA [W;Q] S0^T
   uint64_t* bar_d2 = bars + 8;   // MMA K^T U^
-  uint64_t* bar_dq = bars + 9;   // MMA Q S0^T
-  uint64_t* bar_pu = bars + 10;  // MMA P U
-  uint64_t* ev_w = bars + 11;    // prep -> chain: W tile of the chunk ready
-  uint64_t* ev_sh = bars + 12;   // chain -> prep: bf16 state tile of the chunk ready
-  uint64_t* ev_s = bars + 13;    // chain -> prep: chunk finished
+  uint64_t* bar_pu = bars + 9;   // MMA P U
+  uint64_t* ev_w = bars + 10;    // prep -> chain: [W;Q] tile of the chunk ready
+  uint64_t* ev_s = bars + 11;    // [2] chain -> prep: chunk finished (one barrier per chunk parity)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 128);
   volatile int* flags = reinterpret_cast<volatile int*>(sm + L::BARS + 132);
   int* scratch = reinterpret_cast<int*>(sm + L::BARS + 160);
@@ -387,12 +387,12 @@ __global__ void __launch_bounds__(NT, 1)
     tmem_relinquish();
   }
   auto rec_of = [&](int c) { return p.rec + ((size_t)(ci.first + c) * p.h_v + h) * kRecBytes; };
-  auto load_kq = [&](int c) {
+  auto load_kq = [&](int c) {  // K into its parity's buffer, Q into the single staging buffer
     const int b = c & 1, t0c = t_begin + c * C;
     mbar_arrive_expect_tx(&bar_kq[b], 32768);
     for (int a = 0; a < 2; ++a) {
-      tma_load_2d(sm + L::KQ + b * 32768 + a * 16384, &map_k, &bar_kq[b], hk * DK + a * 64, t0c);
-      tma_load_2d(sm + L::KQ + b * 32768 + a * 16384 + 8192, &map_q, &bar_kq[b], hk * DK + a * 64, t0c);
+      tma_load_2d(sm + L::KB + b * 16384 + a * 8192, &map_k, &bar_kq[b], hk * DK + a * 64, t0c);
+      tma_load_2d(sm + L::QB + a * 8192, &map_q, &bar_kq[b], hk * DK + a * 64, t0c);
     }
   };
   auto load_r2 = [&](int c) {
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(NT, 1)
     bulk_load(sm + L::R1, rec_of(c), kRecPart1, bar_r1);
   };
   if (tid == 0) {
-    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 13; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
     flags[0] = 0;
     tma_prefetch_desc(&map_q);
@@ -439,16 +439,15 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const uint32_t vcoloff = (uint32_t)(row0 & 63) * 2u;
-  const uint64_t dKQk = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);      // K-major view of [K;Q]
-  const uint64_t dKQmn = sdesc_sw128(smem_u32(sm + L::KQ), 16384, 1024);  // MN-major view of K
+  const uint64_t dKmn = sdesc_sw128(smem_u32(sm + L::KB), 8192, 1024);  // MN-major view of K
   const uint64_t dVT = sdesc_sw128(smem_u32(sm + L::VT) + vcoloff, 8192, 1024);
   const uint64_t dR1 = sdesc_sw128(smem_u32(sm + L::R1), 16, 1024);
-  const uint64_t dR2 = sdesc_sw128(smem_u32(sm + L::R2), 16, 1024);
+  // P as rows 64-127 of an M=128 operand: the view starts 64 rows (8 KB) before each P buffer
+  const uint64_t dR2p = sdesc_sw128(smem_u32(sm + L::R2 - 8192), 16, 1024);
   const uint64_t dWQ = sdesc_sw128(smem_u32(sm + L::WQ), 16, 1024);
   const uint64_t dUHmn = sdesc_sw128(smem_u32(sm + L::UH), 16384, 1024);
   const uint64_t dUT = sdesc_sw128(smem_u32(sm + L::UT), 16, 1024);
   const uint64_t dS32 = sdesc_sw128(smem_u32(sm + L::S32), 16, 1024);
-  const uint64_t dSH = sdesc_sw128(smem_u32(sm + L::SH), 16, 1024);
   // Bounded wait.  After the first timeout every later wait returns at once, so both
   // warp groups run their (uniform) loops to the end and the CTA exits with an error.
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -458,63 +457,70 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (chain) {
     // ============================================================ chain warps
-    const int t = 16 * quad + lane;  // M=64 layout row (lanes 0-15)
+    const int t = 32 * (quad & 1) + lane;  // token of this thread's TMEM lane (lane 32*quad + lane)
+    float gq_prev = 0.f;                   // output gate of token t in the previous chunk (warps 2-3)
+    // warps 2-3: O of chunk cc = gq (Q S0^T) + P U, from rows 64-127 of cc's accumulators
+    auto outputs = [&](int cc) {
+      const uint32_t pb = (uint32_t)(cc & 1) * R;
+      tc_fence_after();
+      float dq[R], pu[R];
+      tmem_ld32(tmem + lane_base + L::cD1 + pb, dq);
+      tmem_ld32(tmem + lane_base + L::cPU + pb, pu);
+      tmem_ld_wait();
+      const int t0c = t_begin + cc * C, n = min(C, t_end - t0c);
+      if (t < n) {
+        __align__(16) __nv_bfloat16 o[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) o[i] = __float2bfloat16_rn(fmaf(gq_prev, dq[i], pu[i]));
+        __nv_bfloat16* dst = p.O + ((size_t)(t0c + t) * p.h_v + h) * DV + row0;
+#pragma unroll
+        for (int i = 0; i < R; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
+      }
+    };
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1;
       const float* gate = reinterpret_cast<const float*>(sm + L::R2 + par * 18432 + (kRecGate - kRecPart1));
       wait(ev_w, par);
-      if (tid == 0) {  // D1w = W S0^T (tf32)
+      if (tid == 0) {  // D1 = [W;Q] S0^T (tf32)
         tc_fence_after();
-        constexpr uint32_t idw = idesc_tf32(64, R);
+        constexpr uint32_t id1 = idesc_tf32(128, R);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          mma_tf32(tmem + L::cD1w, dadd(dWQ, (j >> 2) * 8192 + (j & 3) * 32),
-                   dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), idw, j > 0);
+          mma_tf32(tmem + L::cD1 + par * R, dadd(dWQ, (j >> 2) * 16384 + (j & 3) * 32),
+                   dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, j > 0);
         mma_commit(bar_d1);
       }
-      if (p.write_O) {  // bf16 hi|lo copy of the entering state for Q S0^T (its last reader: Q S0^T of c-1)
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-          const __nv_bfloat16 hi = __float2bfloat16_rn(sreg[i]);
-          *reinterpret_cast<__nv_bfloat16*>(sm + L::SH + kbf16(i, dcol, R)) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(sm + L::SH + R * 256 + kbf16(i, dcol, R)) =
-              __float2bfloat16_rn(sreg[i] - __bfloat162float(hi));
-        }
-        fence_async_smem();
-        group_sync(1);
-        if (tid == 0) mbar_arrive(ev_sh);
-      }
       wait(bar_r2 + par, (c >> 1) & 1);  // factors and P of this chunk
-      wait(bar_d1, par);
-      tc_fence_after();
-      {  // U = U~ - W S0^T (M=64 layout); U^ hi|lo MN-major, U^T tf32
+      if (quad < 2) {  // U = U~ - W S0^T (token t); U^ hi|lo MN-major, U^T tf32
+        wait(bar_d1, par);
+        tc_fence_after();
         float ut[R], dw[R];
         tmem_ld32(tmem + lane_base + L::cU + par * R, ut);
-        tmem_ld32(tmem + lane_base + L::cD1w, dw);
+        tmem_ld32(tmem + lane_base + L::cD1 + par * R, dw);
         tmem_ld_wait();
-        if (lane < 16) {
-          const float sc = gate[64 + t];
-          __align__(16) __nv_bfloat16 hi[R], lo[R];
+        const float sc = gate[64 + t];
+        __align__(16) __nv_bfloat16 hi[R], lo[R];
 #pragma unroll
-          for (int i = 0; i < R; i += 4) {
-            float u4[4];
+        for (int i = 0; i < R; i += 4) {
+          float u4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float u = ut[i + e] - dw[i + e];
-              u4[e] = tf32r(u);
-              const float uh = u * sc;
-              hi[i + e] = __float2bfloat16_rn(uh);
-              lo[i + e] = __float2bfloat16_rn(uh - __bfloat162float(hi[i + e]));
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) *reinterpret_cast<float*>(sm + L::UT + kf32(i + e, t, R)) = u4[e];
+          for (int e = 0; e < 4; ++e) {
+            const float u = ut[i + e] - dw[i + e];
+            u4[e] = tf32r(u);
+            const float uh = u * sc;
+            hi[i + e] = __float2bfloat16_rn(uh);
+            lo[i + e] = __float2bfloat16_rn(uh - __bfloat162float(hi[i + e]));
           }
 #pragma unroll
-          for (int i = 0; i < R; i += 8) {
-            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 128)) = *reinterpret_cast<const uint4*>(hi + i);
-            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lo + i);
-          }
+          for (int e = 0; e < 4; ++e) *reinterpret_cast<float*>(sm + L::UT + kf32(i + e, t, R)) = u4[e];
         }
+#pragma unroll
+        for (int i = 0; i < R; i += 8) {
+          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 128)) = *reinterpret_cast<const uint4*>(hi + i);
+          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lo + i);
+        }
+      } else if (p.write_O && c > 0) {
+        outputs(c - 1);
       }
       fence_async_smem();
       tc_fence_before();
@@ -522,40 +528,25 @@ __global__ void __launch_bounds__(NT, 1)
       if (tid == 0) {  // K^T U^ (state)
         tc_fence_after();
         constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
-        const uint32_t kqo = par * 32768u;
+        const uint32_t ko = par * 16384u;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          mma_bf16(tmem + L::cD2, dadd(dKQmn, kqo + (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, j > 0);
+          mma_bf16(tmem + L::cD2, dadd(dKmn, ko + (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, j > 0);
         mma_commit(bar_d2);
-      } else if (tid == 32 && p.write_O) {  // P U (outputs)
+      } else if (tid == 32 && p.write_O) {  // P U (outputs), P in rows 64-127
         tc_fence_after();
-        constexpr uint32_t idp = idesc_tf32(64, R);
+        constexpr uint32_t idp = idesc_tf32(128, R);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          mma_tf32(tmem + L::cPU, dadd(dR2, par * 18432 + (j >> 2) * 8192 + (j & 3) * 32),
+          mma_tf32(tmem + L::cPU + par * R, dadd(dR2p, par * 18432 + (j >> 2) * 8192 + (j & 3) * 32),
                    dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp, j > 0);
         mma_commit(bar_pu);
       }
-      if (p.write_O) {  // outputs of chunk c while K^T U^ runs
-        wait(bar_pu, par);
-        wait(bar_dq, par);
-        tc_fence_after();
-        float dq[R], pu[R];
-        tmem_ld32(tmem + lane_base + L::cD1q, dq);
-        tmem_ld32(tmem + lane_base + L::cPU, pu);
-        tmem_ld_wait();
-        const int t0c = t_begin + c * C, n = min(C, t_end - t0c);
-        if (lane < 16 && t < n) {
-          const float gq = gate[128 + t];
-          __align__(16) __nv_bfloat16 o[R];
-#pragma unroll
-          for (int i = 0; i < R; ++i) o[i] = __float2bfloat16_rn(fmaf(gq, dq[i], pu[i]));
-          __nv_bfloat16* dst = p.O + ((size_t)(t0c + t) * p.h_v + h) * DV + row0;
-#pragma unroll
-          for (int i = 0; i < R; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
-        }
-      }
       wait(bar_d2, par);
+      if (p.write_O) {  // P U has read P: its buffer may be refilled once the chunk is done
+        wait(bar_pu, par);
+        gq_prev = gate[128 + t];
+      }
       tc_fence_after();
       {  // S <- gamma_C S + K^T U^ (M=128 layout: lane = d_k)
         float d2[R];
@@ -571,11 +562,13 @@ __global__ void __launch_bounds__(NT, 1)
       fence_async_smem();
       tc_fence_before();
       group_sync(1);
-      if (tid == 0) mbar_arrive(ev_s);
+      if (tid == 0) mbar_arrive(&ev_s[par]);
     }
+    if (p.write_O && nch > 0 && quad >= 2) outputs(nch - 1);
   } else {
     // ============================================================ prep warps
-    const bool issW = tid == 128, issU = tid == 192, issQ = tid == 224;
+    const bool issW = tid == 128, issU = tid == 192;
+    const int tp = tid - 128;
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1;
       wait(bar_kq + par, (c >> 1) & 1);
@@ -585,11 +578,11 @@ __global__ void __launch_bounds__(NT, 1)
         constexpr uint32_t idW = idesc_bf16(128, 64, true, false);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_bf16(tmem + L::cW, dadd(dKQmn, par * 32768 + j * 2048), dadd(dR1, kRecMW + j * 32), idW, j > 0);
+          mma_bf16(tmem + L::cW, dadd(dKmn, par * 16384 + j * 2048), dadd(dR1, kRecMW + j * 32), idW, j > 0);
         mma_commit(bar_w);
-      } else if (issU) {  // U~ = [Mb_hi|Mb_lo][V;V]
+      } else if (issU) {  // U~ = [Mb_hi|Mb_lo][V;V] (M=128: rows 64-127 are not used)
         tc_fence_after();
-        constexpr uint32_t idU = idesc_bf16(64, R, false, true);
+        constexpr uint32_t idU = idesc_bf16(128, R, false, true);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           mma_bf16(tmem + L::cU + par * R, dadd(dR1, kRecMB + (j >> 2) * 8192 + (j & 3) * 32),
@@ -600,40 +593,48 @@ __global__ void __launch_bounds__(NT, 1)
       wait(bar_u, par);
       tc_fence_after();
       group_sync(2);
-      if (issU && c + 1 < nch) load_r1(c + 1);   // V and record part 1 are free
-      if (c > 0) wait(bar_d1, (c - 1) & 1);       // the previous W S0^T has read the W tile
-      {  // W^T (M=128 layout: lane = d_k) -> tf32 tile W[t][d]
+      if (issU && c + 1 < nch) load_r1(c + 1);  // V and record part 1 are free
+      if (c > 0) wait(bar_d1, (c - 1) & 1);      // the previous [W;Q] S0^T has read the tile
+      {  // W^T (M=128 layout: lane = d_k) -> tf32 rows 0-63 of the [W;Q] tile
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           float v[32];
           tmem_ld32(tmem + lane_base + L::cW + cc * 32, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) *reinterpret_cast<float*>(sm + L::WQ + kf32(cc * 32 + i, dcol, 64)) = tf32r(v[i]);
+          for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<float*>(sm + L::WQ + kf32(cc * 32 + i, dcol, 128)) = tf32r(v[i]);
+        }
+      }
+      if (p.write_O) {  // Q (bf16, exact in fp32) -> rows 64-127: token tq, d_k atom a
+        const int tq = tp & 63, a = tp >> 6;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::QB + kbf16(tq, a * 64 + ch * 8, 64));
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+          const uint32_t k = a * 64 + ch * 8;
+          *reinterpret_cast<float4*>(sm + L::WQ + kf32(64 + tq, k, 128)) = make_float4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<float4*>(sm + L::WQ + kf32(64 + tq, k + 4, 128)) = make_float4(f[4], f[5], f[6], f[7]);
         }
       }
       fence_async_smem();
       tc_fence_before();
-      if (c > 0) wait(ev_s, (c - 1) & 1);  // the chain has finished chunk c-1
       group_sync(2);
+      // The tile is published before waiting for the chain to finish chunk c-1, so the chain
+      // starts chunk c without a round trip.  ev_s has one barrier per chunk parity, and the
+      // chain cannot finish chunk c+1 before this arrival, so the wait below never finds its
+      // barrier two phases ahead.
       if (issW) mbar_arrive(ev_w);
-      if (issU && c + 1 < nch) {           // buffers of chunk c-1 have no readers left
+      if (c > 0) wait(&ev_s[(c - 1) & 1], ((c - 1) >> 1) & 1);  // the chain has finished chunk c-1
+      if (issU && c + 1 < nch) {  // K of chunk c-1 and the Q staging buffer have no readers left
         load_kq(c + 1);
         if (c >= 1) load_r2(c + 1);
-      }
-      if (p.write_O) {
-        wait(ev_sh, par);
-        if (issQ) {  // Q [S0_hi|S0_lo]^T (bf16) of chunk c
-          tc_fence_after();
-          constexpr uint32_t idq = idesc_bf16(64, R, false, false);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t kk = j & 7;  // K step inside d_k; j >= 8 uses the lo half of the state
-            mma_bf16(tmem + L::cD1q, dadd(dKQk, par * 32768 + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32),
-                     dadd(dSH, (j >> 3) * (R * 256) + (kk >> 2) * (R * 128) + (kk & 3) * 32), idq, j > 0);
-          }
-          mma_commit(bar_dq);
-        }
       }
     }
   }

@@ -67,6 +67,17 @@ struct ChunkInfo {
 __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
                                        int* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (n_seqs == 1) {  // one sequence: no scan over the offsets
+    const int a = cu[0], b = cu[1];
+    const int cnt = (a >= 0 && b >= a && b <= total_tokens) ? chunks_of(b - a) : 0;
+    ChunkInfo r;
+    r.first = seq == 0 ? 0 : cnt;
+    r.total = cnt;
+    r.gc_seq = (gc >= 0 && gc < cnt) ? 0 : -1;
+    r.gc_idx = (gc >= 0 && gc < cnt) ? gc : 0;
+    __syncthreads();
+    return r;
+  }
   if (tid == 0) { scratch[8] = 0; scratch[9] = -1; scratch[10] = 0; }
   __syncthreads();
   int carry = 0;
