@@ -469,12 +469,13 @@ __global__ void __launch_bounds__(NT, 1)
       tmem_ld_wait();
       const int t0c = t_begin + cc * C, n = min(C, t_end - t0c);
       if (t < n) {
-        __align__(16) __nv_bfloat16 o[R];
+        __align__(16) __nv_bfloat162 o[R / 2];
 #pragma unroll
-        for (int i = 0; i < R; ++i) o[i] = __float2bfloat16_rn(fmaf(gq_prev, dq[i], pu[i]));
+        for (int i = 0; i < R; i += 2)
+          o[i / 2] = __floats2bfloat162_rn(fmaf(gq_prev, dq[i], pu[i]), fmaf(gq_prev, dq[i + 1], pu[i + 1]));
         __nv_bfloat16* dst = p.O + ((size_t)(t0c + t) * p.h_v + h) * DV + row0;
 #pragma unroll
-        for (int i = 0; i < R; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i);
+        for (int i = 0; i < R; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i / 2);
       }
     };
     for (int c = 0; c < nch; ++c) {
@@ -499,25 +500,23 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_ld32(tmem + lane_base + L::cD1 + par * R, dw);
         tmem_ld_wait();
         const float sc = gate[64 + t];
-        __align__(16) __nv_bfloat16 hi[R], lo[R];
+        // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
+        __align__(16) uint32_t hp[R / 2], lp[R / 2];
 #pragma unroll
-        for (int i = 0; i < R; i += 4) {
-          float u4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float u = ut[i + e] - dw[i + e];
-            u4[e] = tf32r(u);
-            const float uh = u * sc;
-            hi[i + e] = __float2bfloat16_rn(uh);
-            lo[i + e] = __float2bfloat16_rn(uh - __bfloat162float(hi[i + e]));
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) *reinterpret_cast<float*>(sm + L::UT + kf32(i + e, t, R)) = u4[e];
+        for (int i = 0; i < R; i += 2) {
+          const float u0 = ut[i] - dw[i], u1 = ut[i + 1] - dw[i + 1];
+          *reinterpret_cast<float*>(sm + L::UT + kf32(i, t, R)) = tf32r(u0);
+          *reinterpret_cast<float*>(sm + L::UT + kf32(i + 1, t, R)) = tf32r(u1);
+          const float h0 = u0 * sc, h1 = u1 * sc;
+          const float t0 = __uint_as_float(__float_as_uint(h0) & 0xffff0000u);
+          const float t1 = __uint_as_float(__float_as_uint(h1) & 0xffff0000u);
+          hp[i / 2] = bf16x2_trunc(t0, t1);
+          lp[i / 2] = bf16x2_trunc(h0 - t0, h1 - t1);
         }
 #pragma unroll
         for (int i = 0; i < R; i += 8) {
-          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 128)) = *reinterpret_cast<const uint4*>(hi + i);
-          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lo + i);
+          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 128)) = *reinterpret_cast<const uint4*>(hp + i / 2);
+          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lp + i / 2);
         }
       } else if (p.write_O && c > 0) {
         outputs(c - 1);

@@ -32,9 +32,15 @@ __host__ __device__ inline int chunks_of(int len) { return (len + C - 1) / C; }
 
 // Round to the nearest tf32 value (ties away from zero); the tensor cores then read it exactly.
 __device__ __forceinline__ float tf32r(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  // nearest tf32 (10 explicit mantissa bits), ties away from zero, by integer arithmetic on the
+  // bit pattern: adding half a tf32 ulp to the magnitude bits carries into the kept bits exactly
+  // when the dropped part is at least half an ulp
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+
+// Upper 16 bits of two floats packed as a bf16 pair (a in the low half): truncation to bf16.
+__device__ __forceinline__ uint32_t bf16x2_trunc(float a, float b) {
+  return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
 }
 
 // Byte offsets inside 128-byte-swizzled tiles (rows of 128 B, 8-row groups of 1024 B).
