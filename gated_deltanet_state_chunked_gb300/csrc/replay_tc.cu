@@ -295,22 +295,22 @@ struct ScanLay {
   static constexpr uint32_t VT = QB + 16384;        // bf16 V atom: 64 tokens x 128 B
   static constexpr uint32_t R1 = VT + 8192;         // record part 1: Mb hi|lo (16 KB), Mw (8 KB)
   static constexpr uint32_t R2 = R1 + kRecPart1;    // 2 buffers of record part 2: P (16 KB), factors (1 KB)
-  static constexpr uint32_t WQ = R2 + 2 * 18432;    // fp32 [W;Q] (128 rows x 4 atoms): W tf32-rounded, Q exact
-  static constexpr uint32_t UH = WQ + 65536;        // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
+  static constexpr uint32_t UH = R2 + 2 * 18432;    // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
   static constexpr uint32_t UT = UH + 16384;        // fp32 U^T (R rows x 2 atoms)
   static constexpr uint32_t S32 = UT + R * 256;     // fp32 state slice (R rows x 4 atoms), tf32-rounded
   static constexpr uint32_t BARS = S32 + R * 512;
   static constexpr uint32_t TOTAL = BARS + 256;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
-  // TMEM columns.  All accumulators use the M=128 layout (lane = row).  [W;Q] S0^T and U~ put
-  // the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127 (Q S0^T; P U is aimed there too).
-  // U~, [W;Q] S0^T and P U have one copy per chunk parity: a chunk's outputs are read back
-  // while the next chunk's MMAs run.
-  static constexpr uint32_t cW = 0, cU = 64, cD1 = 64 + 2 * R, cD2 = 64 + 4 * R, cPU = 64 + 5 * R;
+  // TMEM columns.  All accumulators use the M=128 layout (lane = row).  cWQ holds the fp32
+  // [W;Q] operand of [W;Q] S0^T (lane = token row, column = d_k), read by the MMA straight from
+  // TMEM.  [W;Q] S0^T and U~ put the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127
+  // (Q S0^T; P U is aimed there too).  U~, [W;Q] S0^T and P U have one copy per chunk parity:
+  // a chunk's outputs are read back while the next chunk's MMAs run.
+  static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = 128 + 4 * R, cPU = 128 + 5 * R;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(64 + 7 * R <= TMEM_COLS, "TMEM columns");
+  static_assert(128 + 7 * R <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
-  static_assert(QB % 1024 == 0 && R2 % 1024 == 0 && WQ % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 &&
+  static_assert(QB % 1024 == 0 && R2 % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 &&
                     S32 % 1024 == 0 && R1 >= 8192,
                 "tile alignment");
 };
@@ -444,7 +444,6 @@ __global__ void __launch_bounds__(NT, 1)
   const uint64_t dR1 = sdesc_sw128(smem_u32(sm + L::R1), 16, 1024);
   // P as rows 64-127 of an M=128 operand: the view starts 64 rows (8 KB) before each P buffer
   const uint64_t dR2p = sdesc_sw128(smem_u32(sm + L::R2 - 8192), 16, 1024);
-  const uint64_t dWQ = sdesc_sw128(smem_u32(sm + L::WQ), 16, 1024);
   const uint64_t dUHmn = sdesc_sw128(smem_u32(sm + L::UH), 16384, 1024);
   const uint64_t dUT = sdesc_sw128(smem_u32(sm + L::UT), 16, 1024);
   const uint64_t dS32 = sdesc_sw128(smem_u32(sm + L::S32), 16, 1024);
@@ -482,13 +481,13 @@ __global__ void __launch_bounds__(NT, 1)
       const uint32_t par = c & 1;
       const float* gate = reinterpret_cast<const float*>(sm + L::R2 + par * 18432 + (kRecGate - kRecPart1));
       wait(ev_w, par);
-      if (tid == 0) {  // D1 = [W;Q] S0^T (tf32)
+      if (tid == 0) {  // D1 = [W;Q] S0^T (tf32, [W;Q] read from TMEM: 8 columns per K step)
         tc_fence_after();
         constexpr uint32_t id1 = idesc_tf32(128, R);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          mma_tf32(tmem + L::cD1 + par * R, dadd(dWQ, (j >> 2) * 16384 + (j & 3) * 32),
-                   dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, j > 0);
+          mma_tf32_ts(tmem + L::cD1 + par * R, tmem + L::cWQ + 8 * j,
+                      dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, j > 0);
         mma_commit(bar_d1);
       }
       wait(bar_r2 + par, (c >> 1) & 1);  // factors and P of this chunk
@@ -567,17 +566,17 @@ __global__ void __launch_bounds__(NT, 1)
   } else {
     // ============================================================ prep warps
     const bool issW = tid == 128, issU = tid == 192;
-    const int tp = tid - 128;
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1;
       wait(bar_kq + par, (c >> 1) & 1);
       wait(bar_r1, par);
-      if (issW) {  // W^T = K^T Mw^T (M=128 over d_k, N=64 tokens)
+      if (c > 0) wait(bar_d1, (c - 1) & 1);  // the previous [W;Q] S0^T has read the [W;Q] columns
+      if (issW) {  // W = Mw K into the [W;Q] columns (M=128: rows 64-127 are replaced by Q below)
         tc_fence_after();
-        constexpr uint32_t idW = idesc_bf16(128, 64, true, false);
+        constexpr uint32_t idW = idesc_bf16(128, 128, false, true);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_bf16(tmem + L::cW, dadd(dKmn, par * 16384 + j * 2048), dadd(dR1, kRecMW + j * 32), idW, j > 0);
+          mma_bf16(tmem + L::cWQ, dadd(dR1, kRecMW + j * 32), dadd(dKmn, par * 16384 + j * 2048), idW, j > 0);
         mma_commit(bar_w);
       } else if (issU) {  // U~ = [Mb_hi|Mb_lo][V;V] (M=128: rows 64-127 are not used)
         tc_fence_after();
@@ -593,36 +592,36 @@ __global__ void __launch_bounds__(NT, 1)
       tc_fence_after();
       group_sync(2);
       if (issU && c + 1 < nch) load_r1(c + 1);  // V and record part 1 are free
-      if (c > 0) wait(bar_d1, (c - 1) & 1);      // the previous [W;Q] S0^T has read the tile
-      {  // W^T (M=128 layout: lane = d_k) -> tf32 rows 0-63 of the [W;Q] tile
+      if (quad < 2) {  // W rows (token = TMEM lane) rounded to nearest tf32 in place: the MMA
+                       // reading them from TMEM would otherwise drop the low mantissa bits
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           float v[32];
-          tmem_ld32(tmem + lane_base + L::cW + cc * 32, v);
+          tmem_ld32(tmem + lane_base + L::cWQ + cc * 32, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<float*>(sm + L::WQ + kf32(cc * 32 + i, dcol, 128)) = tf32r(v[i]);
+          for (int i = 0; i < 32; ++i) v[i] = tf32r(v[i]);
+          tmem_st32(tmem + lane_base + L::cWQ + cc * 32, v);
         }
-      }
-      if (p.write_O) {  // Q (bf16, exact in fp32) -> rows 64-127: token tq, d_k atom a
-        const int tq = tp & 63, a = tp >> 6;
+      } else if (p.write_O) {  // Q rows (token 32*(quad-2) + lane): bf16, exact in fp32
+        const int tq = 32 * (quad - 2) + lane;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::QB + kbf16(tq, a * 64 + ch * 8, 64));
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-          float f[8];
+        for (int cc = 0; cc < 4; ++cc) {  // d_k columns [32 cc, 32 cc + 32)
+          float v[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            f[2 * e] = __uint_as_float(w[e] << 16);
-            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::QB + kbf16(tq, cc * 32 + ch * 8, 64));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[ch * 8 + 2 * e] = __uint_as_float(w[e] << 16);
+              v[ch * 8 + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
           }
-          const uint32_t k = a * 64 + ch * 8;
-          *reinterpret_cast<float4*>(sm + L::WQ + kf32(64 + tq, k, 128)) = make_float4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<float4*>(sm + L::WQ + kf32(64 + tq, k + 4, 128)) = make_float4(f[4], f[5], f[6], f[7]);
+          tmem_st32(tmem + lane_base + L::cWQ + cc * 32, v);
         }
       }
-      fence_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       group_sync(2);
       // The tile is published before waiting for the chain to finish chunk c-1, so the chain
