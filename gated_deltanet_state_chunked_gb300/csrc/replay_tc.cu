@@ -206,21 +206,25 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         const float *G2_ = B_ + 64, *Fa_ = B_ + 128, *Fc_ = B_ + 192, *Pa_ = B_ + 256;
         if (row < 64) {
           const int t = row;
+          float av[32];
           if (fact[sl]) {
             const float at = Fa_[t];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int s = half * 32 + i;
-              A_[t * MST + s] = s < t ? at * Fc_[s] * kq[i] : 0.f;
+              av[i] = s < t ? at * Fc_[s] * kq[i] : 0.f;
             }
           } else {
             const float bt = B_[t] * cRk[t], g_t = G2_[t];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int s = half * 32 + i;
-              A_[t * MST + s] = s < t ? bt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i] : 0.f;
+              av[i] = s < t ? bt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i] : 0.f;
             }
           }
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(A_ + t * MST + half * 32 + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
         } else if (p.write_O) {
           const int t = row - 64;
           const int h = hk * G + pair + sl;
@@ -256,15 +260,17 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
       const int t = gt >> 1, s0 = (gt & 1) * 32;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        __align__(16) __nv_bfloat16 bh[8], bl[8], wv[8];
+        __align__(16) uint32_t bh[4], bl[4], wv[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 8; e += 2) {
           const int s = s0 + 8 * c + e;
-          const float m = mmat[t * MST + s];
-          const float mb = m * gB[s];
-          bh[e] = __float2bfloat16_rn(mb);
-          bl[e] = __float2bfloat16_rn(mb - __bfloat162float(bh[e]));
-          wv[e] = __float2bfloat16_rn(mb * gGam[s] * cRk[s]);
+          const float mb0 = mmat[t * MST + s] * gB[s], mb1 = mmat[t * MST + s + 1] * gB[s + 1];
+          // Mb as bf16 hi + lo, both truncated (|error| < 2^-16 |Mb|); Mw rounded to nearest even
+          const float h0 = __uint_as_float(__float_as_uint(mb0) & 0xffff0000u);
+          const float h1 = __uint_as_float(__float_as_uint(mb1) & 0xffff0000u);
+          bh[e / 2] = bf16x2_trunc(h0, h1);
+          bl[e / 2] = bf16x2_trunc(mb0 - h0, mb1 - h1);
+          wv[e / 2] = bf16x2_rne(mb0 * gGam[s] * cRk[s], mb1 * gGam[s + 1] * cRk[s + 1]);
         }
         const int s = s0 + 8 * c;
         *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(bh);

@@ -42,6 +42,14 @@ __device__ __forceinline__ float tf32r(float x) {
 __device__ __forceinline__ uint32_t bf16x2_trunc(float a, float b) {
   return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
 }
+// Two finite floats rounded to the nearest bf16 (ties to even) and packed (a in the low half):
+// adding 0x7fff plus the lowest kept bit to the pattern carries into the kept 16 bits exactly
+// when the dropped half is above one half ulp, or equal to it with an odd kept part.
+__device__ __forceinline__ uint32_t bf16x2_rne(float a, float b) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  const uint32_t ra = ua + 0x7fffu + ((ua >> 16) & 1u), rb = ub + 0x7fffu + ((ub >> 16) & 1u);
+  return __byte_perm(ra, rb, 0x7632);
+}
 
 // Byte offsets inside 128-byte-swizzled tiles (rows of 128 B, 8-row groups of 1024 B).
 // fp32 K-major tile, atoms of 32 elements along K, `rows` rows per atom column.
