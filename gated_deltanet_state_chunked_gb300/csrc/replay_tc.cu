@@ -16,13 +16,15 @@
 //    in parallel: K K^T on tcgen05, the gated A, and M = (I + A)^{-1} on CUDA
 //    cores (32x32 diagonal blocks by forward substitution, then one block merge), written
 //    with beta, G and rk to a per-(chunk, v-head) record in scratch memory.
-//  * chunk_scan_kernel -- one CTA per 32-row slice of d_v of one (tail, v-head)
-//    state, walking the tail's chunks.  Per chunk:
-//      K^T Mw^T           bf16 (computed factor rounded once)            M=128 N=64  K=64
-//      [Mb_hi|Mb_lo][V;V] bf16 hi/lo split of the computed factor        M=128 N=32  K=128
-//      [W;Q] S0^T         tf32 (W and S0 rounded to nearest, Q exact)    M=128 N=32  K=128
-//      [K^T|K^T][U^hi;U^lo] bf16 split of the scaled U                   M=128 N=32  K=128
-//      P U                tf32                                           M=128 N=32  K=64
+//  * chunk_scan_kernel -- one CTA per 32- or 64-row slice of d_v of one (tail, v-head)
+//    state, walking the tail's chunks (R = 32 while all slices fit on the GPU at once, else
+//    64).  Per chunk:
+//      W = Mw K           bf16 (computed factor rounded once)            M=128 N=128 K=64
+//      [Mb_hi|Mb_lo][V;V] bf16 hi/lo split of the computed factor        M=128 N=R   K=128
+//      [W;Q] S0^T         tf32, [W;Q] from TMEM (W and S0 rounded to     M=128 N=R   K=128
+//                         nearest, Q exact)
+//      [K^T|K^T][U^hi;U^lo] bf16 split of the scaled U                   M=128 N=R   K=128
+//      P U                tf32                                           M=128 N=R   K=64
 //    (the M=128 shapes with 64 meaningful rows put them where the epilogue needs them)
 //    all accumulated in fp32 in TMEM; the state slice stays in fp32 registers.
 // Padded tokens past a tail's end get beta = g = 0 (identity transitions).
@@ -310,11 +312,12 @@ struct ScanLay {
   // TMEM columns.  All accumulators use the M=128 layout (lane = row).  cWQ holds the fp32
   // [W;Q] operand of [W;Q] S0^T (lane = token row, column = d_k), read by the MMA straight from
   // TMEM.  [W;Q] S0^T and U~ put the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127
-  // (Q S0^T; P U is aimed there too).  U~, [W;Q] S0^T and P U have one copy per chunk parity:
-  // a chunk's outputs are read back while the next chunk's MMAs run.
+  // (Q S0^T; P U is aimed there too).  U~ and [W;Q] S0^T have one copy per chunk parity: a
+  // chunk's outputs are read back while the next chunk's [W;Q] S0^T runs.  P U has one copy:
+  // the next P U is issued only after the outputs have read it.
   static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = 128 + 4 * R, cPU = 128 + 5 * R;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(128 + 7 * R <= TMEM_COLS, "TMEM columns");
+  static_assert(128 + 6 * R <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
   static_assert(QB % 1024 == 0 && R2 % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 &&
                     S32 % 1024 == 0 && R1 >= 8192,
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(NT, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, ScanParams p) {
   using L = ScanLay<R>;
-  static_assert(R == 32, "one state slice of 32 rows per CTA");
+  static_assert(R == 32 || R == 64, "state slices of 32 or 64 rows per CTA");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
@@ -467,20 +470,24 @@ __global__ void __launch_bounds__(NT, 1)
     // warps 2-3: O of chunk cc = gq (Q S0^T) + P U, from rows 64-127 of cc's accumulators
     auto outputs = [&](int cc) {
       const uint32_t pb = (uint32_t)(cc & 1) * R;
-      tc_fence_after();
-      float dq[R], pu[R];
-      tmem_ld32(tmem + lane_base + L::cD1 + pb, dq);
-      tmem_ld32(tmem + lane_base + L::cPU + pb, pu);
-      tmem_ld_wait();
       const int t0c = t_begin + cc * C, n = min(C, t_end - t0c);
-      if (t < n) {
-        __align__(16) __nv_bfloat162 o[R / 2];
+      tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < R; i += 2)
-          o[i / 2] = __floats2bfloat162_rn(fmaf(gq_prev, dq[i], pu[i]), fmaf(gq_prev, dq[i + 1], pu[i + 1]));
-        __nv_bfloat16* dst = p.O + ((size_t)(t0c + t) * p.h_v + h) * DV + row0;
+      for (int hh = 0; hh < R / 32; ++hh) {  // 32 state rows at a time
+        float dq[32], pu[32];
+        tmem_ld32(tmem + lane_base + L::cD1 + pb + 32 * hh, dq);
+        tmem_ld32(tmem + lane_base + L::cPU + 32 * hh, pu);
+        tmem_ld_wait();
+        if (t < n) {
+          __align__(16) __nv_bfloat162 o[16];
 #pragma unroll
-        for (int i = 0; i < R; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i / 2);
+          for (int i = 0; i < 32; i += 2)
+            o[i / 2] = __floats2bfloat162_rn(fmaf(gq_prev, dq[i], pu[i]), fmaf(gq_prev, dq[i + 1], pu[i + 1]));
+          __nv_bfloat16* dst = p.O + ((size_t)(t0c + t) * p.h_v + h) * DV + row0 + 32 * hh;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8)
+            *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(o + i / 2);
+        }
       }
     };
     for (int c = 0; c < nch; ++c) {
@@ -500,28 +507,33 @@ __global__ void __launch_bounds__(NT, 1)
       if (quad < 2) {  // U = U~ - W S0^T (token t); U^ hi|lo MN-major, U^T tf32
         wait(bar_d1, par);
         tc_fence_after();
-        float ut[R], dw[R];
-        tmem_ld32(tmem + lane_base + L::cU + par * R, ut);
-        tmem_ld32(tmem + lane_base + L::cD1 + par * R, dw);
-        tmem_ld_wait();
         const float sc = gate[64 + t];
-        // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
-        __align__(16) uint32_t hp[R / 2], lp[R / 2];
 #pragma unroll
-        for (int i = 0; i < R; i += 2) {
-          const float u0 = ut[i] - dw[i], u1 = ut[i + 1] - dw[i + 1];
-          *reinterpret_cast<float*>(sm + L::UT + kf32(i, t, R)) = tf32r(u0);
-          *reinterpret_cast<float*>(sm + L::UT + kf32(i + 1, t, R)) = tf32r(u1);
-          const float h0 = u0 * sc, h1 = u1 * sc;
-          const float t0 = __uint_as_float(__float_as_uint(h0) & 0xffff0000u);
-          const float t1 = __uint_as_float(__float_as_uint(h1) & 0xffff0000u);
-          hp[i / 2] = bf16x2_trunc(t0, t1);
-          lp[i / 2] = bf16x2_trunc(h0 - t0, h1 - t1);
-        }
+        for (int hh = 0; hh < R / 32; ++hh) {  // 32 state rows at a time
+          float ut[32], dw[32];
+          tmem_ld32(tmem + lane_base + L::cU + par * R + 32 * hh, ut);
+          tmem_ld32(tmem + lane_base + L::cD1 + par * R + 32 * hh, dw);
+          tmem_ld_wait();
+          // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
+          __align__(16) uint32_t hp[16], lp[16];
 #pragma unroll
-        for (int i = 0; i < R; i += 8) {
-          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 128)) = *reinterpret_cast<const uint4*>(hp + i / 2);
-          *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lp + i / 2);
+          for (int i = 0; i < 32; i += 2) {
+            const int r = 32 * hh + i;
+            const float u0 = ut[i] - dw[i], u1 = ut[i + 1] - dw[i + 1];
+            *reinterpret_cast<float*>(sm + L::UT + kf32(r, t, R)) = tf32r(u0);
+            *reinterpret_cast<float*>(sm + L::UT + kf32(r + 1, t, R)) = tf32r(u1);
+            const float h0 = u0 * sc, h1 = u1 * sc;
+            const float t0 = __uint_as_float(__float_as_uint(h0) & 0xffff0000u);
+            const float t1 = __uint_as_float(__float_as_uint(h1) & 0xffff0000u);
+            hp[i / 2] = bf16x2_trunc(t0, t1);
+            lp[i / 2] = bf16x2_trunc(h0 - t0, h1 - t1);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            const int r = 32 * hh + i;
+            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, t, 128)) = *reinterpret_cast<const uint4*>(hp + i / 2);
+            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lp + i / 2);
+          }
         }
       } else if (p.write_O && c > 0) {
         outputs(c - 1);
@@ -542,7 +554,7 @@ __global__ void __launch_bounds__(NT, 1)
         constexpr uint32_t idp = idesc_tf32(128, R);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          mma_tf32(tmem + L::cPU + par * R, dadd(dR2p, par * 18432 + (j >> 2) * 8192 + (j & 3) * 32),
+          mma_tf32(tmem + L::cPU, dadd(dR2p, par * 18432 + (j >> 2) * 8192 + (j & 3) * 32),
                    dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp, j > 0);
         mma_commit(bar_pu);
       }
@@ -553,14 +565,18 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc_fence_after();
       {  // S <- gamma_C S + K^T U^ (M=128 layout: lane = d_k)
-        float d2[R];
-        tmem_ld32(tmem + lane_base + L::cD2, d2);
-        tmem_ld_wait();
         const float gC = gate[63];
 #pragma unroll
-        for (int i = 0; i < R; ++i) {
-          sreg[i] = fmaf(gC, sreg[i], d2[i]);
-          *reinterpret_cast<float*>(sm + L::S32 + kf32(i, dcol, R)) = tf32r(sreg[i]);
+        for (int hh = 0; hh < R / 32; ++hh) {
+          float d2[32];
+          tmem_ld32(tmem + lane_base + L::cD2 + 32 * hh, d2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int r = 32 * hh + i;
+            sreg[r] = fmaf(gC, sreg[r], d2[i]);
+            *reinterpret_cast<float*>(sm + L::S32 + kf32(r, dcol, R)) = tf32r(sreg[r]);
+          }
         }
       }
       fence_async_smem();
@@ -697,9 +713,14 @@ cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 }  // namespace
 
 int replay_tc_rows(int n_seqs, int h_v) {
-  (void)n_seqs;
-  (void)h_v;
-  return 32;  // 4 slices of 32 state rows per (tail, v-head)
+  // 4 slices of 32 state rows per (tail, v-head) while those fit on the GPU at once (latency);
+  // 2 slices of 64 rows when there are more (throughput: the MMAs of a chunk take about as long
+  // at N = 64 as at N = 32, so a 64-row CTA does twice the work in a little more time).
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  return (long long)n_seqs * h_v * (DV / 32) > sms ? 64 : 32;
 }
 
 bool replay_tc_supported(const SimtParams& p) {
@@ -741,7 +762,8 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   sp.cu = p.cu; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
   sp.status = p.status; sp.n_seqs = p.n_seqs; sp.total_tokens = p.total_tokens; sp.h_k = p.h_k; sp.h_v = p.h_v;
   sp.write_O = p.write_O;
-  return launch_scan<32>(mq, mk, mv, sp, stream);
+  return replay_tc_rows(p.n_seqs, p.h_v) == 64 ? launch_scan<64>(mq, mk, mv, sp, stream)
+                                                : launch_scan<32>(mq, mk, mv, sp, stream);
 }
 
 }  // namespace gdn
