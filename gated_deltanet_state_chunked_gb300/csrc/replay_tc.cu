@@ -112,6 +112,20 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
   const int t0 = p.cu[ci.gc_seq] + ci.gc_idx * C;
   const int n = min(C, p.cu[ci.gc_seq + 1] - t0);
   const int G = p.h_v / p.h_k;
+  // g and beta of the first slot pair, fetched now so that their latency overlaps the loads
+  // and the Gram below (warp 0 of each warpgroup: tokens lane and lane + 32 of its slot)
+  float pre[4] = {0.f, 0.f, 0.f, 0.f};
+  if ((warp & 3) == 0 && half < min(2, G)) {
+    const int h = hk * G + half;
+    if (lane < n) {
+      pre[0] = p.g[(size_t)(t0 + lane) * p.h_v + h];
+      pre[2] = p.beta[(size_t)(t0 + lane) * p.h_v + h];
+    }
+    if (lane + 32 < n) {
+      pre[1] = p.g[(size_t)(t0 + lane + 32) * p.h_v + h];
+      pre[3] = p.beta[(size_t)(t0 + lane + 32) * p.h_v + h];
+    }
+  }
 
   if (warp == 0) {
     tmem_alloc(tmem_slot, 64);
@@ -176,10 +190,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // gates of both slots: warp 0 of each warpgroup
     if ((warp & 3) == 0 && slot < nslots) {
       const int h = hk * G + pair + slot;
-      float ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-      float gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
-      const float ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-      const float bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+      float ga = pre[0], gb = pre[1], ba = pre[2], bb = pre[3];
+      if (pair > 0) {
+        ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+        gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+        ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+        bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+      }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float xa = __shfl_up_sync(0xffffffffu, ga, o);
@@ -259,22 +276,29 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
       // record: Mb hi|lo, Mw, per-token factors
       const int h = hk * G + pair + slot;
       unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes;
-      const int t = gt >> 1, s0 = (gt & 1) * 32;
+      // item (row t, columns [s, s + 8)): a quarter-warp writes whole 128-byte rows
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int it = 0; it < 4; ++it) {
+        const int t = 16 * it + (gt >> 3), s = 8 * (gt & 7);
+        const float4 m0 = *reinterpret_cast<const float4*>(mmat + t * MST + s);
+        const float4 m1 = *reinterpret_cast<const float4*>(mmat + t * MST + s + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(gB + s), b1 = *reinterpret_cast<const float4*>(gB + s + 4);
+        const float4 y0 = *reinterpret_cast<const float4*>(gGam + s), y1 = *reinterpret_cast<const float4*>(gGam + s + 4);
+        const float4 r0 = *reinterpret_cast<const float4*>(cRk + s), r1 = *reinterpret_cast<const float4*>(cRk + s + 4);
+        const float mb[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
+                             m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
+        const float wf[8] = {y0.x * r0.x, y0.y * r0.y, y0.z * r0.z, y0.w * r0.w,
+                             y1.x * r1.x, y1.y * r1.y, y1.z * r1.z, y1.w * r1.w};
         __align__(16) uint32_t bh[4], bl[4], wv[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-          const int s = s0 + 8 * c + e;
-          const float mb0 = mmat[t * MST + s] * gB[s], mb1 = mmat[t * MST + s + 1] * gB[s + 1];
           // Mb as bf16 hi + lo, both truncated (|error| < 2^-16 |Mb|); Mw rounded to nearest even
-          const float h0 = __uint_as_float(__float_as_uint(mb0) & 0xffff0000u);
-          const float h1 = __uint_as_float(__float_as_uint(mb1) & 0xffff0000u);
+          const float h0 = __uint_as_float(__float_as_uint(mb[e]) & 0xffff0000u);
+          const float h1 = __uint_as_float(__float_as_uint(mb[e + 1]) & 0xffff0000u);
           bh[e / 2] = bf16x2_trunc(h0, h1);
-          bl[e / 2] = bf16x2_trunc(mb0 - h0, mb1 - h1);
-          wv[e / 2] = bf16x2_rne(mb0 * gGam[s] * cRk[s], mb1 * gGam[s + 1] * cRk[s + 1]);
+          bl[e / 2] = bf16x2_trunc(mb[e] - h0, mb[e + 1] - h1);
+          wv[e / 2] = bf16x2_rne(mb[e] * wf[e], mb[e + 1] * wf[e + 1]);
         }
-        const int s = s0 + 8 * c;
         *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(bh);
         *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, 64 + s, 64)) = *reinterpret_cast<const uint4*>(bl);
         *reinterpret_cast<uint4*>(rec + kRecMW + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(wv);
