@@ -137,12 +137,66 @@ __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 
 
 constexpr int MST = 68;  // row stride (floats) of the 64x64 fp32 work matrices (16-byte aligned rows)
 
+// One warp-level tensor-core product D(16x8) += A(16x8) B(8x8), tf32 inputs, fp32 accumulate
+// (the legacy mma.sync path: enough for 32x32 blocks that are too small for tcgen05).
+// Fragments: A rows g and g+8, columns q and q+4; B rows q and q+4, column g; D rows g and
+// g+8, columns 2q and 2q+1 (g = lane / 4, q = lane % 4).
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// x = hi + lo with hi = x truncated to tf32 (low 13 mantissa bits cleared); lo is exact in fp32
+// and is itself read as tf32 by the product, so hi*hi' + hi*lo' + lo*hi' carries about 21
+// significant bits.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// D = sign * L R for 32x32 blocks of stride MST, by one 128-thread warpgroup (t = thread index
+// in it): warp w computes rows [16 (w / 2), +16) and columns [16 (w % 2), +16) with three
+// tf32 products per 8x8 step (split operands).
+__device__ inline void block_mm32(const float* L, const float* Rm, float* D, float sign, int t) {
+  const int w = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
+  const int r0 = 16 * (w >> 1), c0 = 16 * (w & 1);
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int k0 = 0; k0 < 32; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32(L[(r0 + g) * MST + k0 + q], ah[0], al[0]);
+    split_tf32(L[(r0 + g + 8) * MST + k0 + q], ah[1], al[1]);
+    split_tf32(L[(r0 + g) * MST + k0 + q + 4], ah[2], al[2]);
+    split_tf32(L[(r0 + g + 8) * MST + k0 + q + 4], ah[3], al[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int n = c0 + 8 * nt + g;
+      uint32_t bh[2], bl[2];
+      split_tf32(Rm[(k0 + q) * MST + n], bh[0], bl[0]);
+      split_tf32(Rm[(k0 + q + 4) * MST + n], bh[1], bl[1]);
+      mma_m16n8k8_tf32(acc[nt], al, bh);
+      mma_m16n8k8_tf32(acc[nt], ah, bl);
+      mma_m16n8k8_tf32(acc[nt], ah, bh);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int c = c0 + 8 * nt + 2 * q;
+    *reinterpret_cast<float2*>(D + (r0 + g) * MST + c) = make_float2(sign * acc[nt][0], sign * acc[nt][1]);
+    *reinterpret_cast<float2*>(D + (r0 + g + 8) * MST + c) = make_float2(sign * acc[nt][2], sign * acc[nt][3]);
+  }
+}
+
 // M = (I + A)^{-1} for a 64x64 strictly lower A (stride MST), by one 128-thread warpgroup
 // (t = thread index in the group, bid = its named barrier).  In 32x32 blocks,
 //   M11 = (I + A11)^{-1}, M22 = (I + A22)^{-1}, M21 = -M22 A21 M11, M12 = 0:
 // the diagonal blocks by forward substitution with one column per thread held in registers
-// (each row of A is a broadcast load), then the two products with 8 outputs per thread.  A's
-// upper-right block (zero, unused afterwards) holds A21 M11 in between.
+// (each row of A is a broadcast load), then the two products on the warp-level tensor cores
+// in split tf32 (about fp32 accuracy).  A's upper-right block (zero, unused afterwards) holds
+// A21 M11 in between.
 __device__ inline void invert_unit_lower(float* A, float* M, int t, int bid) {
   if (t < 64) {
     const int b = t >> 5, j = t & 31;
@@ -171,38 +225,9 @@ __device__ inline void invert_unit_lower(float* A, float* M, int t, int bid) {
       *reinterpret_cast<float4*>(M + (i >> 3) * MST + 32 + (i & 7) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   group_sync(bid);
-  const int r = t >> 2, c8 = (t & 3) * 8;  // output rows r of a 32x32 block, columns [c8, c8 + 8)
-  {  // X = A21 M11 -> A[0:32][32:64]
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float a = A[(32 + r) * MST + k];
-      const float4 m0 = *reinterpret_cast<const float4*>(M + k * MST + c8);
-      const float4 m1 = *reinterpret_cast<const float4*>(M + k * MST + c8 + 4);
-      x[0] = fmaf(a, m0.x, x[0]); x[1] = fmaf(a, m0.y, x[1]); x[2] = fmaf(a, m0.z, x[2]); x[3] = fmaf(a, m0.w, x[3]);
-      x[4] = fmaf(a, m1.x, x[4]); x[5] = fmaf(a, m1.y, x[5]); x[6] = fmaf(a, m1.z, x[6]); x[7] = fmaf(a, m1.w, x[7]);
-    }
-    *reinterpret_cast<float4*>(A + r * MST + 32 + c8) = make_float4(x[0], x[1], x[2], x[3]);
-    *reinterpret_cast<float4*>(A + r * MST + 32 + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
-  }
+  block_mm32(A + 32 * MST, M, A + 32, 1.f, t);           // X = A21 M11 -> A[0:32][32:64]
   group_sync(bid);
-  {  // M21 = -M22 X
-    float y[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float mm = M[(32 + r) * MST + 32 + k];
-      const float4 x0 = *reinterpret_cast<const float4*>(A + k * MST + 32 + c8);
-      const float4 x1 = *reinterpret_cast<const float4*>(A + k * MST + 32 + c8 + 4);
-      y[0] = fmaf(mm, x0.x, y[0]); y[1] = fmaf(mm, x0.y, y[1]); y[2] = fmaf(mm, x0.z, y[2]); y[3] = fmaf(mm, x0.w, y[3]);
-      y[4] = fmaf(mm, x1.x, y[4]); y[5] = fmaf(mm, x1.y, y[5]); y[6] = fmaf(mm, x1.z, y[6]); y[7] = fmaf(mm, x1.w, y[7]);
-    }
-    *reinterpret_cast<float4*>(M + (32 + r) * MST + c8) = make_float4(-y[0], -y[1], -y[2], -y[3]);
-    *reinterpret_cast<float4*>(M + (32 + r) * MST + c8 + 4) = make_float4(-y[4], -y[5], -y[6], -y[7]);
-  }
+  block_mm32(M + 32 * MST + 32, A + 32, M + 32 * MST, -1.f, t);  // M21 = -M22 X
   group_sync(bid);
 }
 
