@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = warp >> 2;
   const int gc = blockIdx.x, hk = blockIdx.y;
+  grid_dep_launch();  // the scan may start launching once every prep CTA is running
   const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, -1, gc, scratch);
   if (gc >= ci.total || ci.gc_seq < 0) return;
   const int t0 = p.cu[ci.gc_seq] + ci.gc_idx * C;
@@ -445,13 +446,15 @@ __global__ void __launch_bounds__(NT, 1)
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
+    if (nch > 0) load_kq(0);
+    grid_dep_wait();  // the records are written by the prep kernel
     if (nch > 0) {
-      load_kq(0);
       load_r1(0);
       load_r2(0);
     }
     if (nch > 1) load_r2(1);
   }
+  grid_dep_wait();
 
   // entering state (chain warps): thread owns d = 32*quad + lane and all R columns, fp32 registers
   const int dcol = 32 * quad + lane;
@@ -726,12 +729,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
 
 template <int R>
 cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ScanParams& sp,
-                        cudaStream_t stream) {
+                        bool overlap_prep, cudaStream_t stream) {
   using L = ScanLay<R>;
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::ALLOC);
   if (e != cudaSuccess) return e;
-  chunk_scan_kernel<R><<<dim3(DV / R, sp.h_v, sp.n_seqs), NT, L::ALLOC, stream>>>(mq, mk, mv, sp);
-  return cudaGetLastError();
+  // With overlap_prep the scan is a programmatic dependent of the prep kernel just before it on
+  // the stream: its CTAs launch while the last prep CTAs run, set up and fetch the first K, Q
+  // tiles, then wait for the prep grid before reading the records.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(DV / R, sp.h_v, sp.n_seqs);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap_prep ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_scan_kernel<R>, mq, mk, mv, sp);
 }
 
 }  // namespace
@@ -777,7 +792,9 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   chunk_prep_kernel<<<dim3(chunks_ub, p.h_k), NT, PrepLay::ALLOC, stream>>>(mq, mk, pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  bool overlap = true;  // a stage event between the kernels asks for them to run one after the other
   if (void* ev = take_stage_event()) {
+    overlap = false;
     e = cudaEventRecord(static_cast<cudaEvent_t>(ev), stream);
     if (e != cudaSuccess) return e;
   }
@@ -786,8 +803,8 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   sp.cu = p.cu; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
   sp.status = p.status; sp.n_seqs = p.n_seqs; sp.total_tokens = p.total_tokens; sp.h_k = p.h_k; sp.h_v = p.h_v;
   sp.write_O = p.write_O;
-  return replay_tc_rows(p.n_seqs, p.h_v) == 64 ? launch_scan<64>(mq, mk, mv, sp, stream)
-                                                : launch_scan<32>(mq, mk, mv, sp, stream);
+  return replay_tc_rows(p.n_seqs, p.h_v) == 64 ? launch_scan<64>(mq, mk, mv, sp, overlap, stream)
+                                                : launch_scan<32>(mq, mk, mv, sp, overlap, stream);
 }
 
 }  // namespace gdn

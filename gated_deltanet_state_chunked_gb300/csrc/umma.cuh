@@ -66,6 +66,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return true;
 }
 
+// Programmatic dependent launch: a primary grid lets its dependent grid start launching; the
+// dependent waits for the primary grid's completion (and memory) before reading its results.
+// Both are no-ops for grids launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_async_smem() {  // generic-proxy smem writes -> async proxy (MMA/TMA)
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
