@@ -47,6 +47,7 @@ def parse_args():
     ap.add_argument("--precise", action="store_true", help="bf16 inputs on the fp32 CUDA-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-depth", type=int, default=3, help="streams and buffer sets in the host-buffer pipeline")
     ap.add_argument("--no-rows", action="store_true", help="skip the varlen / full / chunk-operator / compose rows")
     return ap.parse_args()
 
@@ -432,25 +433,26 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         # End to end through gdn_replay with host buffers: every step uploads its inputs from
-        # pinned host memory, replays, and reads O and S back.  Two streams and two device buffer
-        # sets, so that step i+1's upload overlaps step i's replay and read-back (as a server
-        # would pipeline requests); the timed region spans all K steps.
+        # pinned host memory, replays, and reads O and S back.  NB streams and device buffer
+        # sets in rotation, so that later steps' uploads overlap a step's replay and read-back
+        # (as a server would pipeline requests); the timed region spans all K steps.
         hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a)).to(dt).pin_memory() for a in (x.q, x.k, x.v))
         hg, hb = (torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in (x.g, x.beta))
         hcu = torch.from_numpy(x.cu_seqlens.astype(np.int32)).pin_memory()
-        hO = [torch.empty(O.shape, dtype=dt).pin_memory() for _ in range(2)]
-        hS = [torch.empty(S.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+        NB = args.e2e_depth
+        hO = [torch.empty(O.shape, dtype=dt).pin_memory() for _ in range(NB)]
+        hS = [torch.empty(S.shape, dtype=torch.float32).pin_memory() for _ in range(NB)]
         sets = []
-        for b in range(2):
+        for b in range(NB):
             sets.append(dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v), g=torch.empty_like(g),
                              beta=torch.empty_like(beta), cu=torch.empty_like(cu), O=torch.empty_like(O),
                              S=torch.empty_like(S)))
-        streams = [stream, torch.cuda.Stream(dev)]
+        streams = [stream] + [torch.cuda.Stream(dev) for _ in range(NB - 1)]
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hcu))
         d2h = hO[0].numel() * hO[0].element_size() + hS[0].numel() * hS[0].element_size()
 
         def e2e_step(i):
-            b = i % 2
+            b = i % NB
             st, bs = streams[b], sets[b]
             with torch.cuda.stream(st):
                 for name, src in (("q", hq), ("k", hk), ("v", hv), ("g", hg), ("beta", hb), ("cu", hcu)):
@@ -463,11 +465,14 @@ def run_ours(args):
         def e2e_run(n):
             t0, t1, j1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             t0.record(streams[0])
-            streams[1].wait_event(t0)
+            for st in streams[1:]:
+                st.wait_event(t0)
             for i in range(n):
                 e2e_step(i)
-            j1.record(streams[1])
-            streams[0].wait_event(j1)
+            for st in streams[1:]:
+                j = torch.cuda.Event()
+                j.record(st)
+                streams[0].wait_event(j)
             t1.record(streams[0])
             torch.cuda.synchronize(dev)
             return t0.elapsed_time(t1)
@@ -484,7 +489,7 @@ def run_ours(args):
             e2e_ms = float(t.item())
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "pipelining": "2 streams, 2 buffer sets: upload of step i+1 overlaps replay and read-back of step i"}
+               "pipelining": f"{NB} streams, {NB} buffer sets: uploads of later steps overlap a step's replay and read-back"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
