@@ -260,7 +260,7 @@ int gdn_compose(const gdn_dims* dims, int32_t K, const float* const* T, const fl
   p.S_in = S_in; p.S_out = S_out; p.K = K; p.h = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
   p.status = device_status_word();
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_compose_simt(p, st);
+  cudaError_t e = compose_tc_supported(p) ? launch_compose_tc(p, st) : launch_compose_simt(p, st);
   if (e != cudaSuccess) return cuda_fail(e, "gdn_compose launch");
   return GDN_OK;
 }

@@ -60,6 +60,9 @@ struct ComposeParams {
 };
 
 cudaError_t launch_compose_simt(const ComposeParams& p, cudaStream_t stream);
+// Tensor-core composition (split tf32, fp32 accuracy) for d_k = d_v = 128 and K >= 1.
+bool compose_tc_supported(const ComposeParams& p);
+cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t stream);
 
 // Sticky status word of the current device (device pointer).
 int* device_status_word();
