@@ -322,7 +322,9 @@ def measure_rows(dev, flush, peaks, replay_us):
     fl = K * x.h_v * 2 * x.d_v * x.d_k * x.d_k
     rows["compose"] = {"K": K, "heads": x.h_v, "d": x.d_k, "us": us, "algorithmic_bytes": by,
                        "gbs": by / (us * 1e-6) / 1e9, "hbm_frac": by / (us * 1e-6) / 1e9 / hbm,
-                       "algorithmic_flops": fl, "path": "fp32 CUDA cores"}
+                       "algorithmic_flops": fl,
+                       "path": "tcgen05 tensor cores, split tf32 (fp32 accuracy)" if x.d_k == 128 and x.d_v == 128
+                       else "fp32 CUDA cores"}
     api.gdn_get_status()
     return rows
 

@@ -143,6 +143,29 @@ def test_compose_matches_oracle_closed_form():
     assert rel_err(host(out0), oracle.compose(T, Sl, None)) <= TOL_F32
 
 
+@pytest.mark.parametrize("K", [0, 1, 2])
+def test_compose_edge_counts(K):
+    """K = 0 copies S_in (or writes zeros); K = 1 and 2 exercise the first and last step of the
+    tensor-core composition (128-dim heads) on their own."""
+    rng = np.random.Generator(np.random.PCG64(40 + K))
+    h, d = 3, 128
+    T = (rng.standard_normal((K, h, d, d)) / np.sqrt(d)).astype(np.float32)
+    Sl = rng.standard_normal((K, h, d, d)).astype(np.float32)
+    S_in = rng.standard_normal((h, d, d)).astype(np.float32)
+    Td = [torch.from_numpy(T[j]).cuda() for j in range(K)]
+    Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
+    out = api.gdn_compose(Td, Sd, torch.from_numpy(S_in).cuda())
+    torch.cuda.synchronize()
+    assert rel_err(host(out), oracle.compose(T, Sl, S_in)) <= TOL_F32
+    if K == 0:  # nothing to compose and no entering state: the binding refuses
+        with pytest.raises(ValueError):
+            api.gdn_compose(Td, Sd, None)
+    else:
+        out0 = api.gdn_compose(Td, Sd, None)
+        torch.cuda.synchronize()
+        assert rel_err(host(out0), oracle.compose(T, Sl, None)) <= TOL_F32
+
+
 def test_composed_chunks_equal_sequential_replay():
     """LinearKV composition passage: composing isolated-chunk operators is exact, so
     compose(chunk operators) on the GPU equals the GPU's own sequential replay."""
