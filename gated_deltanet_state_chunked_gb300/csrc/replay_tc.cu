@@ -146,6 +146,31 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Gate sums of a slot (warp 0 of its warpgroup; tokens lane and lane + 32): inclusive sums G
+  // in log2 units, exp2(G - G_last) and exp2(G_last - G).  For the first pair they are formed
+  // here, while the K, Q tiles are in flight.
+  struct GateSums {
+    float la, lb, ea, eb, fa, fb, ba, bb;
+  };
+  auto gate_sums = [&](float ga, float gb, float ba, float bb) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float xa = __shfl_up_sync(0xffffffffu, ga, o);
+      const float xb = __shfl_up_sync(0xffffffffu, gb, o);
+      if (lane >= o) { ga += xa; gb += xb; }
+    }
+    gb += __shfl_sync(0xffffffffu, ga, 31);
+    GateSums r;
+    r.la = ga * kLog2e;
+    r.lb = gb * kLog2e;
+    const float last = __shfl_sync(0xffffffffu, r.lb, 31);
+    r.ea = exp2f(r.la - last); r.eb = exp2f(r.lb - last);
+    r.fa = exp2f(last - r.la); r.fb = exp2f(last - r.lb);
+    r.ba = ba; r.bb = bb;
+    return r;
+  };
+  GateSums gs0 = {};
+  if ((warp & 3) == 0 && half < min(2, G)) gs0 = gate_sums(pre[0], pre[1], pre[2], pre[3]);
   bool ok = mbar_wait(bar_tma, 0, kWaitNs);
   if (tid == 0) {
     const uint64_t d = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);
@@ -191,22 +216,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // gates of both slots: warp 0 of each warpgroup
     if ((warp & 3) == 0 && slot < nslots) {
       const int h = hk * G + pair + slot;
-      float ga = pre[0], gb = pre[1], ba = pre[2], bb = pre[3];
+      GateSums q = gs0;
       if (pair > 0) {
-        ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-        gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
-        ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-        bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+        const float ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+        const float gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+        const float ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+        const float bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+        q = gate_sums(ga, gb, ba, bb);
       }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float xa = __shfl_up_sync(0xffffffffu, ga, o);
-        const float xb = __shfl_up_sync(0xffffffffu, gb, o);
-        if (lane >= o) { ga += xa; gb += xb; }
-      }
-      gb += __shfl_sync(0xffffffffu, ga, 31);
-      const float la = ga * kLog2e, lb = gb * kLog2e, last = __shfl_sync(0xffffffffu, lb, 31);
-      const float ea = exp2f(la - last), eb = exp2f(lb - last), fa = exp2f(last - la), fb = exp2f(last - lb);
+      const float la = q.la, lb = q.lb, ea = q.ea, eb = q.eb, fa = q.fa, fb = q.fb, ba = q.ba, bb = q.bb;
+      const float last = __shfl_sync(0xffffffffu, lb, 31);
       gB[lane] = ba; gB[lane + 32] = bb;
       gG2[lane] = la; gG2[lane + 32] = lb;
       gFa[lane] = ba * cRk[lane] * ea; gFa[lane + 32] = bb * cRk[lane + 32] * eb;
@@ -247,8 +266,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             *reinterpret_cast<float4*>(A_ + t * MST + half * 32 + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
         } else if (p.write_O) {
           const int t = row - 64;
-          const int h = hk * G + pair + sl;
-          unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP;
+          float* Pst = reinterpret_cast<float*>(ss_ + L::MMAT);  // staging: the slot's M area, free until the inverse
           float x[32];
           if (fact[sl]) {
             const float at = Pa_[t];
@@ -267,11 +285,22 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
           }
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(rec + kf32(t, half * 32 + i, 64)) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+            *reinterpret_cast<float4*>(Pst + t * MST + half * 32 + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
         }
       }
     }
     __syncthreads();
+    if (p.write_O && slot < nslots) {  // P from the staging area to the record, a 128-byte line per quarter warp
+      const int h = hk * G + pair + slot;
+      unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int c = it * 128 + gt, t = c >> 4, a = (c >> 3) & 1, j = c & 7;
+        const float4 v = *reinterpret_cast<const float4*>(mmat + t * MST + a * 32 + j * 4);
+        *reinterpret_cast<float4*>(rec + kf32(t, a * 32 + j * 4, 64)) = v;
+      }
+      group_sync(1 + slot);  // the inverse overwrites the staging area
+    }
     if (slot < nslots) {
       invert_unit_lower(amat, mmat, gt, 1 + slot);
       // record: Mb hi|lo, Mw, per-token factors
@@ -375,10 +404,10 @@ __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d 
 //   D1 = [W;Q] S0^T -> U = U~ - W S0^T, U^ -> D2 = K^T U^ (state), P U (outputs) -> S = gamma_C S + D2.
 // Warps 0-1 form U from the token rows 0-63 of D1 while warps 2-3 write the previous chunk's
 // outputs from rows 64-127 (Q S0^T) and P U, so the output epilogue is off the chunk-to-chunk
-// chain.  Warps 4-7 ("prep") run one chunk ahead: the W^T and U~ MMAs, the fp32 [W;Q] tile
-// and all loads.  The groups hand over through mbarriers that complete once per chunk; MMAs
-// are issued by threads in different warps so that independent streams do not queue behind
-// one issuer.
+// chain.  Warps 4-7 ("prep") run one chunk ahead: the W = Mw K and U~ MMAs, the [W;Q]
+// operand in TMEM (W rounded to tf32 in place, the Q rows stored beside it) and all loads.
+// The groups hand over through mbarriers that complete once per chunk; MMAs are issued by
+// threads in different warps so that independent streams do not queue behind one issuer.
 template <int R>
 __global__ void __launch_bounds__(NT, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -391,12 +420,12 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_kq = bars + 0;   // [2] loads of K and Q
   uint64_t* bar_r2 = bars + 2;   // [2] loads of record part 2
   uint64_t* bar_r1 = bars + 4;   // V + record part 1
-  uint64_t* bar_w = bars + 5;    // MMA W^T
+  uint64_t* bar_w = bars + 5;    // MMA W = Mw K
   uint64_t* bar_u = bars + 6;    // MMA U~
   uint64_t* bar_d1 = bars + 7;   // MMA [W;Q] S0^T
   uint64_t* bar_d2 = bars + 8;   // MMA K^T U^
   uint64_t* bar_pu = bars + 9;   // MMA P U
-  uint64_t* ev_w = bars + 10;    // prep -> chain: [W;Q] tile of the chunk ready
+  uint64_t* ev_w = bars + 10;    // prep -> chain: [W;Q] operand of the chunk ready in TMEM
   uint64_t* ev_s = bars + 11;    // [2] chain -> prep: chunk finished (one barrier per chunk parity)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 128);
   volatile int* flags = reinterpret_cast<volatile int*>(sm + L::BARS + 132);
