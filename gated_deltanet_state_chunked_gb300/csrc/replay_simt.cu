@@ -35,9 +35,11 @@ namespace {
 
 constexpr int C = kChunk;
 constexpr int RS = 32;                // state rows per CTA
-constexpr int KST = kMaxHead + 1;     // row stride of K/Q/S tiles (floats): column reads across rows hit distinct banks
-constexpr int VST = RS + 1;           // row stride of V/R/U tiles
-constexpr int GST = C + 1;            // row stride of the 64x64 tiles
+// Row strides (floats) chosen for the m16n8k8 fragments: rows 4 (K/Q/S, 64x64) or 8 (V/R/U)
+// banks apart, so the eight rows and four columns a fragment load touches hit distinct banks.
+constexpr int KST = kMaxHead + 4;     // K/Q/S tiles
+constexpr int VST = RS + 8;           // V/R/U/X tiles
+constexpr int GST = C + 4;            // the 64x64 tiles
 constexpr int NT = 256;
 
 struct Smem {
@@ -55,6 +57,20 @@ struct Smem {
   float beta[C];
   int scratch[20];
 };
+
+// The C fragments of a warp's two 16 x 8 tiles (rows m0.., columns n0 + [0, 16)) into a
+// row-major tile with row stride ld.
+__device__ __forceinline__ void store_tile(float* T, int ld, const float (&acc)[2][4], int m0, int n0, int lane) {
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int c = n0 + 8 * j + 2 * q;
+    T[(m0 + g) * ld + c] = acc[j][0];
+    T[(m0 + g) * ld + c + 1] = acc[j][1];
+    T[(m0 + g + 8) * ld + c] = acc[j][2];
+    T[(m0 + g + 8) * ld + c + 1] = acc[j][3];
+  }
+}
 
 __device__ __forceinline__ float ld_in(const float* p, size_t i) { return p[i]; }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
@@ -330,23 +346,12 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
         sm.beta[tid] = R[REC_BETA + tid];
       }
       __syncthreads();
-      {  // X = K S0^T: this thread's chunk rows t0x .. t0x + 3, slice rows rx, rx + 1
-        const int rx = (tid % 16) * 2, t0x = (tid / 16) * 4;
-        float x[4][2] = {};
-        for (int d = 0; d < DK; ++d) {
-          const float s0 = sm.S[rx * KST + d], s1 = sm.S[(rx + 1) * KST + d];
-#pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            const float kv = sm.K[(t0x + a) * KST + d];
-            x[a][0] = fmaf(kv, s0, x[a][0]);
-            x[a][1] = fmaf(kv, s1, x[a][1]);
-          }
-        }
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          sm.X[(t0x + a) * VST + rx] = x[a][0];
-          sm.X[(t0x + a) * VST + rx + 1] = x[a][1];
-        }
+      {  // X = K S0^T (64 x 32, K = d_k): warp w -> rows 16 (w / 2), columns 16 (w % 2) + [0, 16)
+        const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 1), n0 = 16 * (w & 1);
+        float acc[2][4] = {};
+        tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.K[m * KST + kk]; },
+                                [&](int kk, int nn) { return sm.S[nn * KST + kk]; }, m0, n0, 0, DK, RS);
+        store_tile(sm.X, VST, acc, m0, n0, lane);
       }
       __syncthreads();
     } else {
@@ -480,47 +485,61 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     }
     __syncthreads();
 
-    // ---- U = M R   (into X, then copied back into V)
-    for (int i = tid; i < C * RS; i += NT) {
-      const int t = i / RS, r = i % RS;
-      float acc = 0.f;
-      for (int s = 0; s <= t; ++s) acc = fmaf(sm.M[t * GST + s], sm.V[s * VST + r], acc);
-      sm.X[t * VST + r] = acc;
+    // ---- U = M R (into X, then copied back into V); M is lower triangular
+    {
+      const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 1), n0 = 16 * (w & 1);
+      float acc[2][4] = {};
+      tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.M[m * GST + kk]; },
+                              [&](int kk, int nn) { return sm.V[kk * VST + nn]; }, m0, n0, 0, m0 + 16, RS);
+      store_tile(sm.X, VST, acc, m0, n0, lane);
     }
     __syncthreads();
     for (int i = tid; i < C * RS; i += NT) sm.V[(i / RS) * VST + (i % RS)] = sm.X[(i / RS) * VST + (i % RS)];
     __syncthreads();
 
-    // ---- outputs O = diag(gamma) Q S0^T + P U, and the new state (into registers)
+    // ---- outputs O = diag(gamma) Q S0^T + P U (P lower triangular)
     if (p.write_O) {
       Tin* O = static_cast<Tin*>(p.O);
-      for (int i = tid; i < C * RS; i += NT) {
-        const int t = i / RS, r = i % RS, rg = row0 + r;
-        if (t >= n || rg >= DV) continue;
-        float acc = 0.f;
-        for (int d = 0; d < DK; ++d) acc = fmaf(sm.Q[t * KST + d], sm.S[r * KST + d], acc);
-        acc *= sm.gam[t];
-        for (int s = 0; s <= t; ++s) acc = fmaf(sm.P[t * GST + s], sm.V[s * VST + r], acc);
-        st_out(O, ((size_t)(t0 + t) * p.h_v + h) * DV + rg, acc);
+      const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 1), n0 = 16 * (w & 1);
+      const int g = lane >> 2, q4 = lane & 3;
+      float acc[2][4] = {};
+      tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.Q[m * KST + kk]; },
+                              [&](int kk, int nn) { return sm.S[nn * KST + kk]; }, m0, n0, 0, DK, RS);
+      const float ga = sm.gam[m0 + g], gb = sm.gam[m0 + g + 8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        acc[j][0] *= ga; acc[j][1] *= ga; acc[j][2] *= gb; acc[j][3] *= gb;
       }
+      tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.P[m * GST + kk]; },
+                              [&](int kk, int nn) { return sm.V[kk * VST + nn]; }, m0, n0, 0, m0 + 16, RS);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = m0 + g + 8 * (e >> 1), rg = row0 + n0 + 8 * j + 2 * q4 + (e & 1);
+          if (t < n && rg < DV) st_out(O, ((size_t)(t0 + t) * p.h_v + h) * DV + rg, acc[j][e]);
+        }
     }
-    constexpr int PER = RS * kMaxHead / NT;  // 16 state entries per thread: rows r0 + 2 e, column d
-    const int sd = tid % kMaxHead, r0 = tid / kMaxHead;
-    float snew[PER];
-    if (sd < DK) {
+    // ---- new state: S <- gamma_C S + (diag(wend) U)^T K (32 x d_k, K = 64 tokens):
+    //      warp w -> rows 16 (w / 4), columns 32 (w % 4) + [0, 32)
+    {
+      const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 2), n0 = 32 * (w & 3);
+      const int g = lane >> 2, q4 = lane & 3;
+      float acc[4][4] = {};
+      tcp::warp_mma_tf32x3<4>(acc, [&](int m, int kk) { return sm.wend[kk] * sm.V[kk * VST + m]; },
+                              [&](int kk, int nn) { return sm.K[kk * KST + nn]; }, m0, n0, 0, C, DK);
       const float gC = sm.gam[C - 1];
+      __syncthreads();  // every read of the entering state (X, outputs) is done
 #pragma unroll
-      for (int e = 0; e < PER; ++e) snew[e] = gC * sm.S[(r0 + 2 * e) * KST + sd];
-      for (int t = 0; t < C; ++t) {
-        const float wk = sm.wend[t] * sm.K[t * KST + sd];
+      for (int j = 0; j < 4; ++j) {
+        const int d = n0 + 8 * j + 2 * q4;
+        if (d >= DK) continue;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) snew[e] = fmaf(sm.V[t * VST + r0 + 2 * e], wk, snew[e]);
+        for (int e = 0; e < 4; ++e) {
+          float* sp = &sm.S[(m0 + g + 8 * (e >> 1)) * KST + d + (e & 1)];
+          *sp = fmaf(gC, *sp, acc[j][e]);
+        }
       }
-    }
-    __syncthreads();
-    if (sd < DK) {
-#pragma unroll
-      for (int e = 0; e < PER; ++e) sm.S[(r0 + 2 * e) * KST + sd] = snew[e];
     }
   }
   __syncthreads();

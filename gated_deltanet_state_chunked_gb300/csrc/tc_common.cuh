@@ -157,6 +157,42 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
   lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
+// As split_tf32 with hi the nearest tf32 value of x (ties away from zero): |lo| <= 2^-11 |x|.
+__device__ __forceinline__ void split_tf32_rn(float x, uint32_t& hi, uint32_t& lo) {
+  const float h = tf32r(x);
+  hi = __float_as_uint(h);
+  lo = __float_as_uint(x - h);
+}
+
+// One warp: acc[j] (the 16 x 8 tile at rows [m0, m0 + 16), columns [n0 + 8 j, +8)) += the sum
+// over k in [k_lo, k_hi) (multiples of 8) of a(m, k) b(k, n), on the warp-level tensor cores in
+// split tf32 (hi = nearest tf32, lo = the rest; lo*hi' + hi*lo' + hi*hi', about 21 bits).
+// Tiles with n0 + 8 j >= n_lim are skipped.  a and b read shared memory; the fragments follow
+// the m16n8k8 layout (see mma_m16n8k8_tf32).
+template <int NTL, typename FA, typename FB>
+__device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[NTL][4], FA a, FB b, int m0, int n0, int k_lo,
+                                                int k_hi, int n_lim) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32_rn(a(m0 + g, k0 + q), ah[0], al[0]);
+    split_tf32_rn(a(m0 + g + 8, k0 + q), ah[1], al[1]);
+    split_tf32_rn(a(m0 + g, k0 + q + 4), ah[2], al[2]);
+    split_tf32_rn(a(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
+#pragma unroll
+    for (int j = 0; j < NTL; ++j) {
+      const int n = n0 + 8 * j;
+      if (n >= n_lim) continue;
+      uint32_t bh[2], bl[2];
+      split_tf32_rn(b(k0 + q, n + g), bh[0], bl[0]);
+      split_tf32_rn(b(k0 + q + 4, n + g), bh[1], bl[1]);
+      mma_m16n8k8_tf32(acc[j], al, bh);
+      mma_m16n8k8_tf32(acc[j], ah, bl);
+      mma_m16n8k8_tf32(acc[j], ah, bh);
+    }
+  }
+}
+
 // D = sign * L R for 32x32 blocks of stride MST, by one 128-thread warpgroup (t = thread index
 // in it): warp w computes rows [16 (w / 2), +16) and columns [16 (w % 2), +16) with three
 // tf32 products per 8x8 step (split operands).
