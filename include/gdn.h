@@ -52,7 +52,7 @@ extern "C" {
 #define GDN_ERR_ARG (-1)         /* null pointer, negative size, bad flag */
 #define GDN_ERR_SHAPE (-2)       /* inconsistent sizes (h_v % h_k, token ranges) */
 #define GDN_ERR_ALIGN (-3)       /* a base pointer breaks the alignment rule */
-#define GDN_ERR_UNSUPPORTED (-4) /* a head size or dtype this build has no kernel for */
+#define GDN_ERR_UNSUPPORTED (-4) /* a head size or dtype the library has no kernel for */
 #define GDN_ERR_CUDA (-5)        /* a CUDA runtime call failed (message in gdn_last_error) */
 #define GDN_ERR_TIMEOUT (-6)     /* a bounded device-side wait gave up */
 #define GDN_ERR_NOMEM (-7)       /* the scratch pool could not grow */
