@@ -314,7 +314,7 @@ def measure_rows(dev, flush, peaks, replay_us):
     fl = x.total_tokens * x.h_v * (6 * x.d_k * rows_aug + 64 * (6 * x.d_k + 4 * rows_aug))
     rows["chunk_operator"] = {"chunks": K, "chunk_tokens": 2048, "heads": x.h_v, "dtype": "f32", "us": us,
                               "algorithmic_flops": fl, "tflops": fl / (us * 1e-6) / 1e12,
-                              "path": "fp32 CUDA cores"}
+                              "path": "fp32 inputs; contractions in split tf32 on warp-level mma.sync"}
     Tl, Sll = [T[j] for j in range(K)], [Sl[j] for j in range(K)]
     SK = torch.empty((x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
     us = _timed_us(lambda: api.gdn_compose(Tl, Sll, None, S_out=SK), flush, 10)
