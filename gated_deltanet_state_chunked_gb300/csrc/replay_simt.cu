@@ -262,6 +262,12 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     if (p.rec) {
       // ---- chunk-shared quantities from the record; keys (and queries) scaled by their norms
       const float* R = reinterpret_cast<const float*>(p.rec) + ((size_t)(first + ck) * p.h_v + h) * REC_FLOATS;
+      float gam_t = 0.f, wend_t = 0.f, beta_t = 0.f;  // issued with the chunk's other loads
+      if (tid < C) {
+        gam_t = R[REC_GAM + tid];
+        wend_t = R[REC_WEND + tid];
+        beta_t = R[REC_BETA + tid];
+      }
       bool vec = false;
       if constexpr (sizeof(Tin) == 4) vec = (DK == kMaxHead) && (DV % RS == 0);
       if (vec) {
@@ -341,9 +347,9 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
       }
       }
       if (tid < C) {
-        sm.gam[tid] = R[REC_GAM + tid];
-        sm.wend[tid] = R[REC_WEND + tid];
-        sm.beta[tid] = R[REC_BETA + tid];
+        sm.gam[tid] = gam_t;
+        sm.wend[tid] = wend_t;
+        sm.beta[tid] = beta_t;
       }
       __syncthreads();
       {  // X = K S0^T (64 x 32, K = d_k): warp w -> rows 16 (w / 2), columns 16 (w % 2) + [0, 16)
@@ -485,16 +491,21 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     }
     __syncthreads();
 
-    // ---- U = M R (into X, then copied back into V); M is lower triangular
+    // ---- U = M R into X (M lower triangular), and diag(wend) U into the A area (free once M
+    //      is known) for the state update
     {
       const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 1), n0 = 16 * (w & 1);
       float acc[2][4] = {};
       tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.M[m * GST + kk]; },
                               [&](int kk, int nn) { return sm.V[kk * VST + nn]; }, m0, n0, 0, m0 + 16, RS);
       store_tile(sm.X, VST, acc, m0, n0, lane);
+      const float wa = sm.wend[m0 + (lane >> 2)], wb = sm.wend[m0 + (lane >> 2) + 8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        acc[j][0] *= wa; acc[j][1] *= wa; acc[j][2] *= wb; acc[j][3] *= wb;
+      }
+      store_tile(sm.A, VST, acc, m0, n0, lane);
     }
-    __syncthreads();
-    for (int i = tid; i < C * RS; i += NT) sm.V[(i / RS) * VST + (i % RS)] = sm.X[(i / RS) * VST + (i % RS)];
     __syncthreads();
 
     // ---- outputs O = diag(gamma) Q S0^T + P U (P lower triangular)
@@ -511,7 +522,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
         acc[j][0] *= ga; acc[j][1] *= ga; acc[j][2] *= gb; acc[j][3] *= gb;
       }
       tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.P[m * GST + kk]; },
-                              [&](int kk, int nn) { return sm.V[kk * VST + nn]; }, m0, n0, 0, m0 + 16, RS);
+                              [&](int kk, int nn) { return sm.X[kk * VST + nn]; }, m0, n0, 0, m0 + 16, RS);
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -526,7 +537,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
       const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 2), n0 = 32 * (w & 3);
       const int g = lane >> 2, q4 = lane & 3;
       float acc[4][4] = {};
-      tcp::warp_mma_tf32x3<4>(acc, [&](int m, int kk) { return sm.wend[kk] * sm.V[kk * VST + m]; },
+      tcp::warp_mma_tf32x3<4>(acc, [&](int m, int kk) { return sm.A[kk * VST + m]; },
                               [&](int kk, int nn) { return sm.K[kk * KST + nn]; }, m0, n0, 0, C, DK);
       const float gC = sm.gam[C - 1];
       __syncthreads();  // every read of the entering state (X, outputs) is done

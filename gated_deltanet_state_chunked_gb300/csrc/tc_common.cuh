@@ -173,6 +173,7 @@ template <int NTL, typename FA, typename FB>
 __device__ __forceinline__ void warp_mma_tf32x3(float (&acc)[NTL][4], FA a, FB b, int m0, int n0, int k_lo,
                                                 int k_hi, int n_lim) {
   const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll 4
   for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
     uint32_t ah[4], al[4];
     split_tf32_rn(a(m0 + g, k0 + q), ah[0], al[0]);
