@@ -140,10 +140,10 @@ void gdn_set_stage_event(void* event) { g_stage_event = event; }
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 size_t gdn_workspace_bytes(const gdn_dims* dims) {
-  if (!dims || dims->dtype != GDN_BF16 || (dims->flags & GDN_PRECISE) || dims->d_k != kMaxHead ||
-      dims->d_v != kMaxHead || dims->total_tokens <= 0 || dims->n_seqs <= 0 || dims->h_v <= 0)
-    return 0;
-  return replay_tc_workspace_bytes(dims->n_seqs, dims->total_tokens, dims->h_v);
+  if (!dims || dims->total_tokens <= 0 || dims->n_seqs <= 0 || dims->h_v <= 0) return 0;
+  if (dims->dtype == GDN_BF16 && !(dims->flags & GDN_PRECISE) && dims->d_k == kMaxHead && dims->d_v == kMaxHead)
+    return replay_tc_workspace_bytes(dims->n_seqs, dims->total_tokens, dims->h_v);
+  return simt_records_bytes(dims->n_seqs, dims->total_tokens, dims->h_v);  // fp32 path: its records
 }
 
 int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
@@ -190,8 +190,19 @@ int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v
     if (ef != cudaSuccess) return cuda_fail(ef, "scratch release");
     return GDN_OK;
   }
-  cudaError_t e = launch_replay_simt(p, dims->dtype == GDN_BF16, st);
+  // fp32 path in two passes: the chunk-shared quantities (norms, gates, (I + A)^{-1}, P) once per
+  // (chunk, v-head) into pool scratch, then the row slices of each state read them.
+  const size_t bytes = simt_records_bytes(p.n_seqs, p.total_tokens, p.h_v);
+  cudaMemPool_t pool = nullptr;
+  int prc = scratch_pool(&pool);
+  if (prc) return prc;
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+  if (e != cudaSuccess) return fail(GDN_ERR_NOMEM, "scratch of %zu bytes: %s", bytes, cudaGetErrorString(e));
+  e = launch_replay_simt_two_pass(p, dims->dtype == GDN_BF16, ws, bytes, st);
+  const cudaError_t ef = cudaFreeAsync(ws, st);
   if (e != cudaSuccess) return cuda_fail(e, "gdn_replay launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch release");
   return GDN_OK;
 }
 

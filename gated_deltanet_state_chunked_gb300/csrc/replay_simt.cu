@@ -1,5 +1,7 @@
-// fp32 CUDA-core chunked scan: the precise path of gdn_replay (fp32 inputs,
-// or bf16 inputs with GDN_PRECISE) and the whole of gdn_chunk_operator.
+// fp32 chunked scan: the precise path of gdn_replay (fp32 inputs, other head
+// sizes, or bf16 inputs with GDN_PRECISE) and the whole of gdn_chunk_operator.
+// fp32 data throughout; the contractions run on warp-level tensor cores
+// (mma.sync) in split tf32, about 21 significant bits.
 //
 // Method: "Tail-Replay: Escaping the Curse of Linear Attention in Prefix
 // Caching for Hybrid LLMs", section 2 Eq. (1) and section 3 Eq. (2), run
@@ -22,8 +24,10 @@
 // (right-multiplied form) = T_C^T, written transposed as T_C.
 //
 // One CTA owns a 32-row slice of one (sequence, v-head) state and walks its
-// chunks; the chunk-shared quantities (Gram matrices, M) are recomputed per
-// slice.  Partial last chunks are padded with tokens that have k = 0,
+// chunks.  gdn_replay and gdn_chunk_operator run two passes: the chunk-shared
+// quantities (norms, gates, M, P) once per (chunk, v-head) into a record, then
+// the slices read them; the allocation-free replay computes them in every
+// slice (one pass, no scratch).  Partial last chunks are padded with tokens that have k = 0,
 // beta = 0, g = 0: identity transitions whose outputs are not stored.
 #include <cuda_bf16.h>
 

@@ -92,8 +92,11 @@ typedef struct {
  *                Rows outside every sequence's range are not written.
  *   S_out        fp32 [n_seqs][h_v][d_v][d_k]; may alias S0 (in-place update)
  * Computation: chunks of 64 tokens, fp32 state carried between chunks.  bf16
- * inputs run on the tcgen05 tensor cores; fp32 inputs (or GDN_PRECISE) on
- * fp32 CUDA cores.
+ * inputs with 128-dim heads run on the tcgen05 tensor cores.  fp32 inputs,
+ * other head sizes and GDN_PRECISE take the fp32 path: fp32 data, its
+ * contractions in split tf32 on warp-level tensor cores (about 21 significant
+ * bits), in two passes with pool scratch of (ceil(total_tokens / 64) + n_seqs)
+ * * h_v * 34048 bytes (gdn_workspace_bytes gives the amount).
  */
 int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
                const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
@@ -138,8 +141,8 @@ int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const void* k, const
  *   T_out       fp32 [n_seqs][h_v][d_k][d_k], T_C row-major, so that
  *               S_out = S_in T_C^T + S_local in this ABI's state layout
  *   Slocal_out  fp32 [n_seqs][h_v][d_v][d_k]
- * q is not needed; dims->scale and GDN_STATE_ONLY are ignored.  Computed in
- * fp32 on CUDA cores whatever the input dtype, in two passes: the chunk-shared
+ * q is not needed; dims->scale and GDN_STATE_ONLY are ignored.  Computed on
+ * the fp32 path (see gdn_replay) whatever the input dtype, in two passes: the chunk-shared
  * quantities ((I + A)^{-1}, gates, norms) once per (64-token piece, v-head)
  * into pool scratch of (ceil(total_tokens / 64) + n_seqs) * h_v * 34048 bytes,
  * then the row slices of the augmented state.
