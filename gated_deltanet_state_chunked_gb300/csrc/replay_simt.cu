@@ -48,6 +48,7 @@ constexpr int NT = 256;
 
 struct Smem {
   float K[C * KST];
+  float K2[C * KST];   // second key buffer: the next chunk's keys arrive while this one is used
   float Q[C * KST];
   float S[RS * KST];
   float V[C * VST];    // values, then R, then U
@@ -59,8 +60,18 @@ struct Smem {
   float gam[C];        // exp(G_t)
   float wend[C];       // exp(G_last - G_t)
   float beta[C];
+  float rk[C];         // key norm factors of the record path (gam, wend, beta, rk are contiguous)
   int scratch[20];
 };
+
+// 16-byte asynchronous copy global -> shared (zero-filled when !valid; src must still be mapped).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // The C fragments of a warp's two 16 x 8 tiles (rows m0.., columns n0 + [0, 16)) into a
 // row-major tile with row stride ld.
@@ -260,74 +271,84 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     sm.S[r * KST + d] = s;
   }
 
+  // fp32 inputs with 128-dim heads on the record path: each chunk's keys, M, value slice and
+  // gate factors arrive by asynchronous copies issued one chunk (keys) or half a chunk (the
+  // rest) ahead; the keys stay unscaled and their norm factors rk are applied to the products.
+  bool vec = false;
+  if constexpr (sizeof(Tin) == 4) vec = p.rec && (DK == kMaxHead) && (DV % RS == 0);
+  const float* kf = reinterpret_cast<const float*>(k);
+  const float* vf = reinterpret_cast<const float*>(v);
+  auto rec_of = [&](int ck) {
+    return reinterpret_cast<const float*>(p.rec) + ((size_t)(first + ck) * p.h_v + h) * REC_FLOATS;
+  };
+  auto pf_keys = [&](int t0c, int nc, float* kb) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+      const bool ok = t < nc;
+      cp_async16(kb + t * KST + d4, kf + ((size_t)(t0c + (ok ? t : 0)) * p.h_k + hk) * DK + d4, ok);
+    }
+  };
+  auto pf_rest = [&](const float* Rc, int t0c, int nc) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = (tid + j * NT) * 4, t = i / C, s2 = i % C;
+      cp_async16(sm.M + t * GST + s2, Rc + REC_M + i, true);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i4 = tid + j * NT, t = i4 >> 3, r4 = (i4 & 7) * 4;
+      const bool ok = t < nc && row0 + r4 < DV;
+      cp_async16(sm.V + t * VST + r4, ok ? vf + ((size_t)(t0c + t) * p.h_v + h) * DV + row0 + r4 : vf, ok);
+    }
+    if (tid < 64) cp_async16(sm.gam + tid * 4, Rc + REC_GAM + tid * 4, true);  // gam, wend, beta, rk
+  };
+  if (vec && t_begin < t_end) {
+    pf_keys(t_begin, min(C, t_end - t_begin), sm.K);
+    pf_rest(rec_of(0), t_begin, min(C, t_end - t_begin));
+    cp_async_commit();
+  }
+
   for (int t0 = t_begin, ck = 0; t0 < t_end; t0 += C, ++ck) {
     const int n = min(C, t_end - t0);
+    const bool more = t0 + C < t_end;
+    float* const Kc = (vec && (ck & 1)) ? sm.K2 : sm.K;  // this chunk's keys
     __syncthreads();
     if (p.rec) {
       // ---- chunk-shared quantities from the record; keys (and queries) scaled by their norms
-      const float* R = reinterpret_cast<const float*>(p.rec) + ((size_t)(first + ck) * p.h_v + h) * REC_FLOATS;
-      float gam_t = 0.f, wend_t = 0.f, beta_t = 0.f;  // issued with the chunk's other loads
-      if (tid < C) {
-        gam_t = R[REC_GAM + tid];
-        wend_t = R[REC_WEND + tid];
-        beta_t = R[REC_BETA + tid];
-      }
-      bool vec = false;
-      if constexpr (sizeof(Tin) == 4) vec = (DK == kMaxHead) && (DV % RS == 0);
+      const float* R = rec_of(ck);
       if (vec) {
-        // fp32, 128-dim heads: every global load of the chunk issued before the first shared store
-        const float* kf = reinterpret_cast<const float*>(k);
-        const float* qf = reinterpret_cast<const float*>(q);
-        const float* vf = reinterpret_cast<const float*>(v);
-        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 kv[8], qv[8], mv[4], pv[4], vv[2];
-        float rkv[8], rqv[8];
+        cp_async_wait_all();
+        if (p.write_O) {  // queries (scaled by rq) and P, read directly
+          const float* qf = reinterpret_cast<const float*>(q);
+          const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 qv[8], pv[4];
+          float rqv[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
-          const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d4;
-          kv[j] = t < n ? *reinterpret_cast<const float4*>(kf + off) : z4;
-          qv[j] = (t < n && p.write_O) ? *reinterpret_cast<const float4*>(qf + off) : z4;
-          rkv[j] = R[REC_RK + t];
-          rqv[j] = R[REC_RQ + t];
-        }
+          for (int j = 0; j < 8; ++j) {
+            const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+            qv[j] = t < n ? *reinterpret_cast<const float4*>(qf + ((size_t)(t0 + t) * p.h_k + hk) * DK + d4) : z4;
+            rqv[j] = R[REC_RQ + t];
+          }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          mv[j] = *reinterpret_cast<const float4*>(R + REC_M + (tid + j * NT) * 4);
-          pv[j] = p.write_O ? *reinterpret_cast<const float4*>(R + REC_P + (tid + j * NT) * 4) : z4;
-        }
+          for (int j = 0; j < 4; ++j) pv[j] = *reinterpret_cast<const float4*>(R + REC_P + (tid + j * NT) * 4);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int i4 = tid + j * NT, t = i4 >> 3, r4 = (i4 & 7) * 4;
-          vv[j] = (t < n && row0 + r4 < DV)
-                      ? *reinterpret_cast<const float4*>(vf + ((size_t)(t0 + t) * p.h_v + h) * DV + row0 + r4)
-                      : z4;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
-          float* kd = sm.K + t * KST + d4;
-          kd[0] = rkv[j] * kv[j].x; kd[1] = rkv[j] * kv[j].y; kd[2] = rkv[j] * kv[j].z; kd[3] = rkv[j] * kv[j].w;
-          if (p.write_O) {
+          for (int j = 0; j < 8; ++j) {
+            const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
             float* qd = sm.Q + t * KST + d4;
             qd[0] = rqv[j] * qv[j].x; qd[1] = rqv[j] * qv[j].y; qd[2] = rqv[j] * qv[j].z; qd[3] = rqv[j] * qv[j].w;
           }
-        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = (tid + j * NT) * 4, t = i / C, s2 = i % C;
-          float* md = sm.M + t * GST + s2;
-          md[0] = mv[j].x; md[1] = mv[j].y; md[2] = mv[j].z; md[3] = mv[j].w;
-          if (p.write_O) {
+          for (int j = 0; j < 4; ++j) {
+            const int i = (tid + j * NT) * 4, t = i / C, s2 = i % C;
             float* pd = sm.P + t * GST + s2;
             pd[0] = pv[j].x; pd[1] = pv[j].y; pd[2] = pv[j].z; pd[3] = pv[j].w;
           }
         }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int i4 = tid + j * NT, t = i4 >> 3, r4 = (i4 & 7) * 4;
-          float* vd = sm.V + t * VST + r4;
-          vd[0] = vv[j].x; vd[1] = vv[j].y; vd[2] = vv[j].z; vd[3] = vv[j].w;
+        __syncthreads();  // this chunk's copies (issued by every thread) have all landed
+        if (more) {
+          pf_keys(t0 + C, min(C, t_end - t0 - C), (ck & 1) ? sm.K : sm.K2);
+          cp_async_commit();
         }
       } else {
 #pragma unroll 8
@@ -349,18 +370,24 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
         sm.M[t * GST + s2] = R[REC_M + i];
         if (p.write_O) sm.P[t * GST + s2] = R[REC_P + i];
       }
-      }
-      if (tid < C) {
-        sm.gam[tid] = gam_t;
-        sm.wend[tid] = wend_t;
-        sm.beta[tid] = beta_t;
+      if (tid < C) {  // keys stored scaled: rk = 1
+        sm.gam[tid] = R[REC_GAM + tid];
+        sm.wend[tid] = R[REC_WEND + tid];
+        sm.beta[tid] = R[REC_BETA + tid];
+        sm.rk[tid] = 1.f;
       }
       __syncthreads();
-      {  // X = K S0^T (64 x 32, K = d_k): warp w -> rows 16 (w / 2), columns 16 (w % 2) + [0, 16)
+      }
+      {  // X = diag(rk) K S0^T (64 x 32, K = d_k): warp w -> rows 16 (w / 2), columns 16 (w % 2) + [0, 16)
         const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 1), n0 = 16 * (w & 1);
         float acc[2][4] = {};
-        tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.K[m * KST + kk]; },
+        tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return Kc[m * KST + kk]; },
                                 [&](int kk, int nn) { return sm.S[nn * KST + kk]; }, m0, n0, 0, DK, RS);
+        const float ra = sm.rk[m0 + (lane >> 2)], rb = sm.rk[m0 + (lane >> 2) + 8];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          acc[j][0] *= ra; acc[j][1] *= ra; acc[j][2] *= rb; acc[j][3] *= rb;
+        }
         store_tile(sm.X, VST, acc, m0, n0, lane);
       }
       __syncthreads();
@@ -382,6 +409,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
       const bool in = tid < n;
       sm.G[tid] = in ? p.g[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
       sm.beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
+      sm.rk[tid] = 1.f;  // keys are normalised in place below
     }
     __syncthreads();
 
@@ -495,7 +523,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     }
     __syncthreads();
 
-    // ---- U = M R into X (M lower triangular), and diag(wend) U into the A area (free once M
+    // ---- U = M R into X (M lower triangular), and diag(wend rk) U into the A area (free once M
     //      is known) for the state update
     {
       const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 1), n0 = 16 * (w & 1);
@@ -503,7 +531,8 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
       tcp::warp_mma_tf32x3<2>(acc, [&](int m, int kk) { return sm.M[m * GST + kk]; },
                               [&](int kk, int nn) { return sm.V[kk * VST + nn]; }, m0, n0, 0, m0 + 16, RS);
       store_tile(sm.X, VST, acc, m0, n0, lane);
-      const float wa = sm.wend[m0 + (lane >> 2)], wb = sm.wend[m0 + (lane >> 2) + 8];
+      const float wa = sm.wend[m0 + (lane >> 2)] * sm.rk[m0 + (lane >> 2)];
+      const float wb = sm.wend[m0 + (lane >> 2) + 8] * sm.rk[m0 + (lane >> 2) + 8];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         acc[j][0] *= wa; acc[j][1] *= wa; acc[j][2] *= wb; acc[j][3] *= wb;
@@ -535,15 +564,20 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
           if (t < n && rg < DV) st_out(O, ((size_t)(t0 + t) * p.h_v + h) * DV + rg, acc[j][e]);
         }
     }
-    // ---- new state: S <- gamma_C S + (diag(wend) U)^T K (32 x d_k, K = 64 tokens):
+    const float gC = sm.gam[C - 1];
+    if (vec && more) {  // the next chunk's M, value slice and factors: their current readers are done
+      __syncthreads();
+      pf_rest(rec_of(ck + 1), t0 + C, min(C, t_end - t0 - C));
+      cp_async_commit();
+    }
+    // ---- new state: S <- gamma_C S + (diag(wend rk) U)^T K (32 x d_k, K = 64 tokens):
     //      warp w -> rows 16 (w / 4), columns 32 (w % 4) + [0, 32)
     {
       const int w = tid >> 5, lane = tid & 31, m0 = 16 * (w >> 2), n0 = 32 * (w & 3);
       const int g = lane >> 2, q4 = lane & 3;
       float acc[4][4] = {};
       tcp::warp_mma_tf32x3<4>(acc, [&](int m, int kk) { return sm.A[kk * VST + m]; },
-                              [&](int kk, int nn) { return sm.K[kk * KST + nn]; }, m0, n0, 0, C, DK);
-      const float gC = sm.gam[C - 1];
+                              [&](int kk, int nn) { return Kc[kk * KST + nn]; }, m0, n0, 0, C, DK);
       __syncthreads();  // every read of the entering state (X, outputs) is done
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
