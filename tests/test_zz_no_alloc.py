@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from gated_deltanet_state_chunked_gb300 import _lib, api, synthetic
-from tests.gpu_util import TOL_BF16, host, rel_err, to_device
+from tests.gpu_util import TOL_BF16, TOL_F32, host, oracle_replay, rel_err, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,22 @@ def test_matches_gdn_replay_on_two_calls_in_a_row():
         (O, S), (O_ref, S_ref) = _both(x)
         assert rel_err(host(S), host(S_ref)) <= TOL_BF16
         assert rel_err(host(O), host(O_ref)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("d_k,d_v", [(128, 128), (64, 32)])
+def test_fp32_inputs_one_pass_path_matches_the_oracle(d_k, d_v):
+    """fp32 inputs need no scratch here: the fp32 path computes the chunk-shared quantities in
+    every row slice (one pass) instead of reading records.  Checked against the fp64 oracle."""
+    x = synthetic.make_replay_inputs([300, 77, 1], 2, 4, d_k, d_v, dtype="f32", seed=504, with_S0=True)
+    d = to_device(x)
+    O = torch.empty((x.total_tokens, 4, d_v), dtype=torch.float32, device="cuda")
+    S = torch.empty((3, 4, d_v, d_k), dtype=torch.float32, device="cuda")
+    api.gdn_replay_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["S0"], O, S)
+    torch.cuda.synchronize()
+    api.gdn_get_status()
+    S_ref, O_ref = oracle_replay(x)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+    assert rel_err(host(O), O_ref) <= TOL_F32
 
 
 def test_single_layer_3277_token_tail_fits():
