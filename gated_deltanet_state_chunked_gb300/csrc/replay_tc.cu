@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             *reinterpret_cast<float4*>(A_ + t * MST + half * 32 + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
         } else if (p.write_O) {
           const int t = row - 64;
-          float* Pst = reinterpret_cast<float*>(ss_ + L::MMAT);  // staging: the slot's M area, free until the inverse
+          // staged in the record's own layout in the [K;Q] area (free once the Gram and the norms
+          // have read it), 16 KB per slot, then stored by one bulk copy
+          unsigned char* Pst = sm + L::KQ + sl * 16384;
           float x[32];
           if (fact[sl]) {
             const float at = Pa_[t];
@@ -285,21 +287,17 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
           }
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(Pst + t * MST + half * 32 + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+            *reinterpret_cast<float4*>(Pst + kf32(t, half * 32 + i, 64)) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
         }
       }
     }
+    fence_async_smem();  // the staged P -> the bulk copy
     __syncthreads();
-    if (p.write_O && slot < nslots) {  // P from the staging area to the record, a 128-byte line per quarter warp
+    const bool issP = p.write_O && slot < nslots && gt == 0;
+    if (issP) {  // P to the record: one 16 KB bulk copy, in flight during the inverse
       const int h = hk * G + pair + slot;
-      unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP;
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int c = it * 128 + gt, t = c >> 4, a = (c >> 3) & 1, j = c & 7;
-        const float4 v = *reinterpret_cast<const float4*>(mmat + t * MST + a * 32 + j * 4);
-        *reinterpret_cast<float4*>(rec + kf32(t, a * 32 + j * 4, 64)) = v;
-      }
-      group_sync(1 + slot);  // the inverse overwrites the staging area
+      bulk_store(p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP, sm + L::KQ + slot * 16384, 16384);
+      bulk_commit();
     }
     if (slot < nslots) {
       invert_unit_lower(amat, mmat, gt, 1 + slot);
@@ -340,6 +338,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         gate[128 + gt] = gGam[gt] * cRq[gt];
       }
     }
+    if (issP) bulk_wait_all();  // the next pair restages P; the CTA's stores are complete at exit
     __syncthreads();
   }
   tc_fence_before();

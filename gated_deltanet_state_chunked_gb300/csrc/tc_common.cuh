@@ -227,20 +227,54 @@ __device__ inline void block_mm32(const float* L, const float* Rm, float* D, flo
   }
 }
 
+// D = sign * L R for 16x16 blocks of stride MST, by one warp (three tf32 products per 8x8 step,
+// split operands as in block_mm32).
+__device__ inline void block_mm16(const float* L, const float* Rm, float* D, float sign) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int k0 = 0; k0 < 16; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32(L[g * MST + k0 + q], ah[0], al[0]);
+    split_tf32(L[(g + 8) * MST + k0 + q], ah[1], al[1]);
+    split_tf32(L[g * MST + k0 + q + 4], ah[2], al[2]);
+    split_tf32(L[(g + 8) * MST + k0 + q + 4], ah[3], al[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int n = 8 * nt + g;
+      uint32_t bh[2], bl[2];
+      split_tf32(Rm[(k0 + q) * MST + n], bh[0], bl[0]);
+      split_tf32(Rm[(k0 + q + 4) * MST + n], bh[1], bl[1]);
+      mma_m16n8k8_tf32(acc[nt], al, bh);
+      mma_m16n8k8_tf32(acc[nt], ah, bl);
+      mma_m16n8k8_tf32(acc[nt], ah, bh);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int c = 8 * nt + 2 * q;
+    *reinterpret_cast<float2*>(D + g * MST + c) = make_float2(sign * acc[nt][0], sign * acc[nt][1]);
+    *reinterpret_cast<float2*>(D + (g + 8) * MST + c) = make_float2(sign * acc[nt][2], sign * acc[nt][3]);
+  }
+}
+
 // M = (I + A)^{-1} for a 64x64 strictly lower A (stride MST), by one 128-thread warpgroup
-// (t = thread index in the group, bid = its named barrier).  In 32x32 blocks,
-//   M11 = (I + A11)^{-1}, M22 = (I + A22)^{-1}, M21 = -M22 A21 M11, M12 = 0:
-// the diagonal blocks by forward substitution with one column per thread held in registers
-// (each row of A is a broadcast load), then the two products on the warp-level tensor cores
-// in split tf32 (about fp32 accuracy).  A's upper-right block (zero, unused afterwards) holds
-// A21 M11 in between.
+// (t = thread index in the group, bid = its named barrier).  For a unit lower block matrix
+// [[I + X, 0], [Y, I + Z]] the inverse is [[P, 0], [-Q Y P, Q]] with P = (I + X)^{-1},
+// Q = (I + Z)^{-1}; applied twice:
+//  * warps 0 and 1 solve the four 16x16 diagonal blocks by forward substitution, one column
+//    per thread held in registers (each row of A is a broadcast load), and each merges its
+//    pair into a 32x32 diagonal block, while the other two warps clear the upper blocks of M;
+//  * the warpgroup merges those two into M.
+// The products run on the warp-level tensor cores in split tf32 (about fp32 accuracy).  A's
+// upper blocks (zero, unused afterwards) hold the intermediate Y P products.
 __device__ inline void invert_unit_lower(float* A, float* M, int t, int bid) {
   if (t < 64) {
-    const int b = t >> 5, j = t & 31;
-    const float* Ab = A + (32 * b) * MST + 32 * b;
-    float m[32];
+    const int b = t >> 4, j = t & 15;
+    const float* Ab = A + (16 * b) * MST + 16 * b;
+    float m[16];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
+    for (int r = 0; r < 16; ++r) {
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
       for (int s = 0; s + 3 < r; s += 4) {
@@ -256,15 +290,31 @@ __device__ inline void invert_unit_lower(float* A, float* M, int t, int bid) {
       m[r] = r == j ? 1.f : (r < j ? 0.f : x);
     }
 #pragma unroll
-    for (int r = 0; r < 32; ++r) M[(32 * b + r) * MST + 32 * b + j] = m[r];
+    for (int r = 0; r < 16; ++r) M[(16 * b + r) * MST + 16 * b + j] = m[r];
+    // warp w: 32x32 diagonal block w from its two 16x16 blocks (both solved by this warp)
+    __syncwarp();
+    const int o = 32 * (t >> 5);
+    block_mm16(A + (o + 16) * MST + o, M + o * MST + o, A + o * MST + o + 16, 1.f);  // Y P
+    __syncwarp();
+    block_mm16(M + (o + 16) * MST + o + 16, A + o * MST + o + 16, M + (o + 16) * MST + o, -1.f);  // -Q (Y P)
   } else {
-    for (int i = t - 64; i < 256; i += 64)  // M12 = 0
-      *reinterpret_cast<float4*>(M + (i >> 3) * MST + 32 + (i & 7) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    // upper blocks of M: rows 0-31 x columns 32-63, rows 0-15 x 16-31, rows 32-47 x 48-63
+    for (int i = t - 64; i < 384; i += 64) {
+      int row, col;
+      if (i < 256) {
+        row = i >> 3, col = 32 + (i & 7) * 4;
+      } else if (i < 320) {
+        row = (i - 256) >> 2, col = 16 + (i & 3) * 4;
+      } else {
+        row = 32 + ((i - 320) >> 2), col = 48 + (i & 3) * 4;
+      }
+      *reinterpret_cast<float4*>(M + row * MST + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   group_sync(bid);
-  block_mm32(A + 32 * MST, M, A + 32, 1.f, t);           // X = A21 M11 -> A[0:32][32:64]
+  block_mm32(A + 32 * MST, M, A + 32, 1.f, t);                   // A21 M11 -> A[0:32][32:64]
   group_sync(bid);
-  block_mm32(M + 32 * MST + 32, A + 32, M + 32 * MST, -1.f, t);  // M21 = -M22 X
+  block_mm32(M + 32 * MST + 32, A + 32, M + 32 * MST, -1.f, t);  // M21 = -M22 (A21 M11)
   group_sync(bid);
 }
 
