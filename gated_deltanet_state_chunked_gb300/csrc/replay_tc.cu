@@ -293,8 +293,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     }
     fence_async_smem();  // the staged P -> the bulk copy
     __syncthreads();
-    const bool issP = p.write_O && slot < nslots && gt == 0;
-    if (issP) {  // P to the record: one 16 KB bulk copy, in flight during the inverse
+    // P to the record: one 16 KB bulk copy, in flight during the inverse.  Issued by a thread of
+    // warp 3 of the slot, which only clears M's upper blocks before the inverse's first barrier
+    // (issuing can hold a thread for about a thousand cycles).
+    const bool issP = p.write_O && slot < nslots && gt == 96;
+    if (issP) {
       const int h = hk * G + pair + slot;
       bulk_store(p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP, sm + L::KQ + slot * 16384, 16384);
       bulk_commit();
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         gate[128 + gt] = gGam[gt] * cRq[gt];
       }
     }
-    if (issP) bulk_wait_all();  // the next pair restages P; the CTA's stores are complete at exit
+    if (issP) bulk_wait_read_all();  // the next pair restages P; the source stays until read
     __syncthreads();
   }
   tc_fence_before();
