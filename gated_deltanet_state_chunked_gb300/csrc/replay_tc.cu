@@ -354,9 +354,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 // ---------------------------------------------------------------------------------------------
 template <int R>
 struct ScanLay {
-  static constexpr uint32_t KB = 0;                 // 2 buffers of bf16 K: 2 d_k atoms x (64 rows x 128 B)
-  static constexpr uint32_t QB = KB + 32768;        // bf16 Q of the chunk being staged: 2 d_k atoms x (64 rows x 128 B)
-  static constexpr uint32_t VT = QB + 16384;        // bf16 V atom: 64 tokens x 128 B
+  // With 32-row slices K has three buffers and Q two, so that a chunk's K and Q are copied a
+  // whole chunk ahead (the prep warps otherwise wait for them); with 64-row slices (the
+  // throughput case, where that measured slower) K has two and Q one, copied once the chain
+  // has finished the chunk two before.
+  static constexpr bool EARLY_KQ = R == 32;
+  static constexpr int NKB = EARLY_KQ ? 3 : 2, NQB = EARLY_KQ ? 2 : 1;
+  static constexpr uint32_t KB = 0;                 // NKB buffers of bf16 K: 2 d_k atoms x (64 rows x 128 B)
+  static constexpr uint32_t QB = KB + NKB * 16384;  // NQB buffers of bf16 Q: 2 d_k atoms x (64 rows x 128 B)
+  static constexpr uint32_t VT = QB + NQB * 16384;  // bf16 V atom: 64 tokens x 128 B
   static constexpr uint32_t R1 = VT + 8192;         // record part 1: Mb hi|lo (16 KB), Mw (8 KB)
   static constexpr uint32_t R2 = R1 + kRecPart1;    // 2 buffers of record part 2: P (16 KB), factors (1 KB)
   static constexpr uint32_t UH = R2 + 2 * 18432;    // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
@@ -371,9 +377,15 @@ struct ScanLay {
   // (Q S0^T; P U is aimed there too).  U~ and [W;Q] S0^T have one copy per chunk parity: a
   // chunk's outputs are read back while the next chunk's [W;Q] S0^T runs.  P U has one copy:
   // the next P U is issued only after the outputs have read it.
-  static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = 128 + 4 * R, cPU = 128 + 5 * R;
+  // A thread issues small MMAs one after another at a fixed cost each, whatever their size,
+  // while threads in different warps issue side by side; so each product is split by K over
+  // ND1 / ND2 / NPU issuing warps, each into an accumulator of its own, and the epilogues add
+  // the partial sums.  With 64-row slices the columns hold one accumulator per product.
+  static constexpr int ND1 = R == 32 ? 3 : 1, ND2 = R == 32 ? 2 : 1, NPU = R == 32 ? 2 : 1;
+  // accumulator a of [W;Q] S0^T for chunk parity b: cD1 + (2 a + b) R; of K^T U^ and P U: + a R
+  static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = cD1 + 2 * R * ND1, cPU = cD2 + R * ND2;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(128 + 6 * R <= TMEM_COLS, "TMEM columns");
+  static_assert(cPU + R * NPU <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
   static_assert(QB % 1024 == 0 && R2 % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 &&
                     S32 % 1024 == 0 && R1 >= 8192,
@@ -402,6 +414,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // Advance a shared-memory descriptor's start address by a byte offset (multiple of 16).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
+// f(j, j == J0) for j = J0 .. J1-1, unrolled at compile time (an MMA issue loop whose operand
+// offsets fold to constants: each instruction a thread issues costs it many cycles, so the
+// issue loop carries no arithmetic of its own).
+template <int J0, int J1, typename F>
+__device__ __forceinline__ void issue_range(F&& f) {
+#pragma unroll
+  for (int j = J0; j < J1; ++j) f(j, j == J0);
+}
+
 // Warp-specialised scan.  Warps 0-3 ("chain") carry the state from chunk to chunk:
 //   D1 = [W;Q] S0^T -> U = U~ - W S0^T, U^ -> D2 = K^T U^ (state), P U (outputs) -> S = gamma_C S + D2.
 // Warps 0-1 form U from the token rows 0-63 of D1 while warps 2-3 write the previous chunk's
@@ -429,6 +450,9 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_pu = bars + 9;   // MMA P U
   uint64_t* ev_w = bars + 10;    // prep -> chain: [W;Q] operand of the chunk ready in TMEM
   uint64_t* ev_s = bars + 11;    // [2] chain -> prep: chunk finished (one barrier per chunk parity)
+  // buffers of chunk c's K and Q tiles
+  auto kbuf = [&](int c) { return (uint32_t)(c % L::NKB); };
+  auto qbuf = [&](int c) { return (uint32_t)(L::NQB == 2 ? c & 1 : 0); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 128);
   volatile int* flags = reinterpret_cast<volatile int*>(sm + L::BARS + 132);
   int* scratch = reinterpret_cast<int*>(sm + L::BARS + 160);
@@ -452,12 +476,12 @@ __global__ void __launch_bounds__(NT, 1)
     tmem_relinquish();
   }
   auto rec_of = [&](int c) { return p.rec + ((size_t)(ci.first + c) * p.h_v + h) * kRecBytes; };
-  auto load_kq = [&](int c) {  // K into its parity's buffer, Q into the single staging buffer
+  auto load_kq = [&](int c) {
     const int b = c & 1, t0c = t_begin + c * C;
     mbar_arrive_expect_tx(&bar_kq[b], 32768);
     for (int a = 0; a < 2; ++a) {
-      tma_load_2d(sm + L::KB + b * 16384 + a * 8192, &map_k, &bar_kq[b], hk * DK + a * 64, t0c);
-      tma_load_2d(sm + L::QB + a * 8192, &map_q, &bar_kq[b], hk * DK + a * 64, t0c);
+      tma_load_2d(sm + L::KB + kbuf(c) * 16384 + a * 8192, &map_k, &bar_kq[b], hk * DK + a * 64, t0c);
+      tma_load_2d(sm + L::QB + qbuf(c) * 16384 + a * 8192, &map_q, &bar_kq[b], hk * DK + a * 64, t0c);
     }
   };
   auto load_r2 = [&](int c) {
@@ -471,7 +495,10 @@ __global__ void __launch_bounds__(NT, 1)
     bulk_load(sm + L::R1, rec_of(c), kRecPart1, bar_r1);
   };
   if (tid == 0) {
-    for (int i = 0; i < 13; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 13; ++i) {  // the MMA barriers count one commit per issuing thread
+      const int n = &bars[i] == bar_d1 ? L::ND1 : &bars[i] == bar_d2 ? L::ND2 : &bars[i] == bar_pu ? L::NPU : 1;
+      mbar_init(&bars[i], n);
+    }
     mbar_fence_init();
     flags[0] = 0;
     tma_prefetch_desc(&map_q);
@@ -536,6 +563,22 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_ld32(tmem + lane_base + L::cD1 + pb + 32 * hh, dq);
         tmem_ld32(tmem + lane_base + L::cPU + 32 * hh, pu);
         tmem_ld_wait();
+#pragma unroll
+        for (int a = 1; a < L::ND1; ++a) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + L::cD1 + (2 * a) * R + pb + 32 * hh, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dq[i] += x[i];
+        }
+#pragma unroll
+        for (int a = 1; a < L::NPU; ++a) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + L::cPU + a * R + 32 * hh, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pu[i] += x[i];
+        }
         if (t < n) {
           __align__(16) __nv_bfloat162 o[16];
 #pragma unroll
@@ -552,13 +595,20 @@ __global__ void __launch_bounds__(NT, 1)
       const uint32_t par = c & 1;
       const float* gate = reinterpret_cast<const float*>(sm + L::R2 + par * 18432 + (kRecGate - kRecPart1));
       wait(ev_w, par);
-      if (tid == 0) {  // D1 = [W;Q] S0^T (tf32, [W;Q] read from TMEM: 8 columns per K step)
+      if (lane == 0 && warp < L::ND1) {  // D1 = [W;Q] S0^T (tf32, [W;Q] from TMEM: 8 columns per K step)
         tc_fence_after();
         constexpr uint32_t id1 = idesc_tf32(128, R);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          mma_tf32_ts(tmem + L::cD1 + par * R, tmem + L::cWQ + 8 * j,
-                      dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, j > 0);
+        const uint32_t dst = tmem + L::cD1 + (2 * warp + par) * R;
+        auto d1 = [&](int j, bool first) {
+          mma_tf32_ts(dst, tmem + L::cWQ + 8 * j, dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, !first);
+        };
+        if constexpr (L::ND1 == 1) {
+          issue_range<0, 16>(d1);
+        } else {  // K steps 0-4, 5-9, 10-15
+          if (warp == 0) issue_range<0, 5>(d1);
+          else if (warp == 1) issue_range<5, 10>(d1);
+          else issue_range<10, 16>(d1);
+        }
         mma_commit(bar_d1);
       }
       wait(bar_r2 + par, (c >> 1) & 1);  // factors and P of this chunk
@@ -572,6 +622,14 @@ __global__ void __launch_bounds__(NT, 1)
           tmem_ld32(tmem + lane_base + L::cU + par * R + 32 * hh, ut);
           tmem_ld32(tmem + lane_base + L::cD1 + par * R + 32 * hh, dw);
           tmem_ld_wait();
+#pragma unroll
+          for (int a = 1; a < L::ND1; ++a) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + L::cD1 + (2 * a + par) * R + 32 * hh, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dw[i] += x[i];
+          }
           // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
           __align__(16) uint32_t hp[16], lp[16];
 #pragma unroll
@@ -599,21 +657,37 @@ __global__ void __launch_bounds__(NT, 1)
       fence_async_smem();
       tc_fence_before();
       group_sync(1);
-      if (tid == 0) {  // K^T U^ (state)
+      // K^T U^ (state) from warps 0 (and 2), P U (outputs, P in rows 64-127) from warps 1 (and 3)
+      if (lane == 0 && (warp & 1) == 0 && (warp >> 1) < L::ND2) {
         tc_fence_after();
         constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
-        const uint32_t ko = par * 16384u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          mma_bf16(tmem + L::cD2, dadd(dKmn, ko + (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, j > 0);
+        const uint64_t dk = dadd(dKmn, kbuf(c) * 16384u);
+        const uint32_t dst = tmem + L::cD2 + (warp >> 1) * R;
+        auto d2 = [&](int j, bool first) {
+          mma_bf16(dst, dadd(dk, (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, !first);
+        };
+        if constexpr (L::ND2 == 1) {
+          issue_range<0, 8>(d2);
+        } else {
+          if (warp == 0) issue_range<0, 4>(d2);
+          else issue_range<4, 8>(d2);
+        }
         mma_commit(bar_d2);
-      } else if (tid == 32 && p.write_O) {  // P U (outputs), P in rows 64-127
+      } else if (lane == 0 && (warp & 1) == 1 && (warp >> 1) < L::NPU && p.write_O) {
         tc_fence_after();
         constexpr uint32_t idp = idesc_tf32(128, R);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          mma_tf32(tmem + L::cPU, dadd(dR2p, par * 18432 + (j >> 2) * 8192 + (j & 3) * 32),
-                   dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp, j > 0);
+        const uint64_t dp = dadd(dR2p, par * 18432);
+        const uint32_t dst = tmem + L::cPU + (warp >> 1) * R;
+        auto pu = [&](int j, bool first) {
+          mma_tf32(dst, dadd(dp, (j >> 2) * 8192 + (j & 3) * 32), dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp,
+                   !first);
+        };
+        if constexpr (L::NPU == 1) {
+          issue_range<0, 8>(pu);
+        } else {
+          if (warp == 1) issue_range<0, 4>(pu);
+          else issue_range<4, 8>(pu);
+        }
         mma_commit(bar_pu);
       }
       wait(bar_d2, par);
@@ -629,6 +703,14 @@ __global__ void __launch_bounds__(NT, 1)
           float d2[32];
           tmem_ld32(tmem + lane_base + L::cD2 + 32 * hh, d2);
           tmem_ld_wait();
+#pragma unroll
+          for (int a = 1; a < L::ND2; ++a) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + L::cD2 + a * R + 32 * hh, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) d2[i] += x[i];
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int r = 32 * hh + i;
@@ -648,6 +730,11 @@ __global__ void __launch_bounds__(NT, 1)
     const bool issW = tid == 128, issU = tid == 192;
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1;
+      // (three K, two Q buffers) K and Q of chunk c+1, a chunk ahead: K goes to the buffer of
+      // chunk c-2, Q to that of chunk c-1; their readers (W, K^T U^ of c-2; the Q rows of c-1)
+      // finished before the chain ended chunk c-2, which the previous iteration waited for.
+      // bar_kq[(c+1)&1] last completed for chunk c-1, also waited for: no phase overrun.
+      if (L::EARLY_KQ && issU && c + 1 < nch) load_kq(c + 1);
       wait(bar_kq + par, (c >> 1) & 1);
       wait(bar_r1, par);
       if (c > 0) wait(bar_d1, (c - 1) & 1);  // the previous [W;Q] S0^T has read the [W;Q] columns
@@ -656,7 +743,7 @@ __global__ void __launch_bounds__(NT, 1)
         constexpr uint32_t idW = idesc_bf16(128, 128, false, true);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_bf16(tmem + L::cWQ, dadd(dR1, kRecMW + j * 32), dadd(dKmn, par * 16384 + j * 2048), idW, j > 0);
+          mma_bf16(tmem + L::cWQ, dadd(dR1, kRecMW + j * 32), dadd(dKmn, kbuf(c) * 16384 + j * 2048), idW, j > 0);
         mma_commit(bar_w);
       } else if (issU) {  // U~ = [Mb_hi|Mb_lo][V;V] (M=128: rows 64-127 are not used)
         tc_fence_after();
@@ -675,13 +762,18 @@ __global__ void __launch_bounds__(NT, 1)
       if (quad < 2) {  // W rows (token = TMEM lane) rounded to nearest tf32 in place: the MMA
                        // reading them from TMEM would otherwise drop the low mantissa bits
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float v[32];
+        for (int cc = 0; cc < 4; cc += 2) {
+          float v[32], w[32];
           tmem_ld32(tmem + lane_base + L::cWQ + cc * 32, v);
+          tmem_ld32(tmem + lane_base + L::cWQ + cc * 32 + 32, w);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = tf32r(v[i]);
+          for (int i = 0; i < 32; ++i) {
+            v[i] = tf32r(v[i]);
+            w[i] = tf32r(w[i]);
+          }
           tmem_st32(tmem + lane_base + L::cWQ + cc * 32, v);
+          tmem_st32(tmem + lane_base + L::cWQ + cc * 32 + 32, w);
         }
       } else if (p.write_O) {  // Q rows (token 32*(quad-2) + lane): bf16, exact in fp32
         const int tq = 32 * (quad - 2) + lane;
@@ -690,7 +782,7 @@ __global__ void __launch_bounds__(NT, 1)
           float v[32];
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::QB + kbf16(tq, cc * 32 + ch * 8, 64));
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::QB + qbuf(c) * 16384 + kbf16(tq, cc * 32 + ch * 8, 64));
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -710,9 +802,10 @@ __global__ void __launch_bounds__(NT, 1)
       // barrier two phases ahead.
       if (issW) mbar_arrive(ev_w);
       if (c > 0) wait(&ev_s[(c - 1) & 1], ((c - 1) >> 1) & 1);  // the chain has finished chunk c-1
-      if (issU && c + 1 < nch) {  // K of chunk c-1 and the Q staging buffer have no readers left
-        load_kq(c + 1);
-        if (c >= 1) load_r2(c + 1);
+      if (issU && c + 1 < nch) {
+        // (two K, one Q buffer) K of chunk c-1 and the Q staging buffer have no readers left
+        if (!L::EARLY_KQ) load_kq(c + 1);
+        if (c >= 1) load_r2(c + 1);  // P and factors of chunk c-1 are no longer read
       }
     }
   }
