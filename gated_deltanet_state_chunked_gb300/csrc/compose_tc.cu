@@ -13,9 +13,11 @@
 // fp32 accuracy from three tf32 products per step (split operands, x = hi + lo with hi the
 // nearest tf32 value of x and lo = x - hi exact in fp32, read by the MMA as its tf32 part):
 // T_hi S_lo + T_lo S_hi + T_hi S_hi, accumulated in fp32 in TMEM.
-// The 48 MMAs of a step go to two accumulators from two issuing threads (the main product and
-// the two corrections); while they run, the threads hold S_local_{j+1} and T_{j+2} loads in
-// flight (fetched as soon as the previous values have been used).
+// A thread issues small MMAs one after another at a fixed cost each, while threads of
+// different warps issue side by side: the 48 MMAs of a step are spread over four issuing
+// threads (warps 0-3), twelve each, into four accumulators that the epilogue adds.  While they
+// run, the threads hold S_local_{j+1} and T_{j+2} loads in flight (fetched as soon as the
+// previous values have been used).
 #include "tc_common.cuh"
 
 namespace gdn {
@@ -34,8 +36,9 @@ struct CTLay {
   static constexpr uint32_t BARS = 32768;
   static constexpr uint32_t TOTAL = BARS + 64;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
-  // TMEM columns: tf32(T), T - tf32(T), the accumulator
+  // TMEM columns: tf32(T), T - tf32(T), four accumulators of 32 columns
   static constexpr uint32_t cTH = 0, cTL = 128, cD = 256;
+  static constexpr int NACC = 4;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(bar, 2);
+    mbar_init(bar, CTLay::NACC);  // one commit per issuing thread
     mbar_fence_init();
     *flag = 0;
   }
@@ -119,25 +122,41 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
   };
   const uint64_t dBH = sdesc_sw128(smem_u32(sm + L::SBH), 16, 1024);
   const uint64_t dBL = sdesc_sw128(smem_u32(sm + L::SBL), 16, 1024);
-  // two accumulators issued by two threads: tid 0 the main product T_hi S_hi into cD, tid 32
-  // the corrections T_hi S_lo + T_lo S_hi into cD + 32; bar counts both commits
+  // MMA n of a step (0..47): pass n / 16 (T_hi S_lo, T_lo S_hi, T_hi S_hi), K step n % 16
+  auto mma_n = [&](int n, uint32_t dcol, bool first) {
+    constexpr uint32_t id = idesc_tf32(128, CTR);
+    const int pass = n >> 4, kk = n & 15;
+    const uint32_t a = pass == 1 ? L::cTL : L::cTH;
+    const uint64_t b = pass == 0 ? dBL : dBH;
+    mma_tf32_ts(tmem + dcol, tmem + a + 8 * kk, b + (uint64_t)((((kk >> 2) * (CTR * 128)) + (kk & 3) * 32) >> 4), id,
+                !first);
+  };
+  // thread 32 w issues MMAs 12 w .. 12 w + 11 into accumulator w (indices fold to constants)
   auto issue = [&]() {
     tc_fence_after();
-    constexpr uint32_t id = idesc_tf32(128, CTR);
-    const int p0 = tid == 0 ? 2 : 0, p1 = tid == 0 ? 3 : 2;
-    const uint32_t dcol = tid == 0 ? L::cD : L::cD + 32;
-    int n = 0;
-#pragma unroll 1
-    for (int pass = p0; pass < p1; ++pass) {
-      const uint32_t a = pass == 1 ? L::cTL : L::cTH;
-      const uint64_t b = pass == 0 ? dBL : dBH;
+    const int w = tid >> 5;
+    const uint32_t dcol = L::cD + 32 * w;
+    switch (w) {
+      case 0:
 #pragma unroll
-      for (int kk = 0; kk < 16; ++kk, ++n)
-        mma_tf32_ts(tmem + dcol, tmem + a + 8 * kk, b + (uint64_t)((((kk >> 2) * (CTR * 128)) + (kk & 3) * 32) >> 4),
-                    id, n > 0);
+        for (int n = 0; n < 12; ++n) mma_n(n, dcol, n == 0);
+        break;
+      case 1:
+#pragma unroll
+        for (int n = 12; n < 24; ++n) mma_n(n, dcol, n == 12);
+        break;
+      case 2:
+#pragma unroll
+        for (int n = 24; n < 36; ++n) mma_n(n, dcol, n == 24);
+        break;
+      default:
+#pragma unroll
+        for (int n = 36; n < 48; ++n) mma_n(n, dcol, n == 36);
+        break;
     }
     mma_commit(bar);
   };
+  const bool issuer = (tid & 31) == 0 && tid < 32 * L::NACC;
 
   fetch_T(0);
   store_T();
@@ -145,7 +164,7 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 || tid == 32) issue();
+  if (issuer) issue();
   if (p.K > 1) fetch_T(1);
   fetch_L(0);
 
@@ -153,12 +172,14 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     // step j's MMAs done: S_j = D + S_local_j
     if (!mbar_wait(bar, (uint32_t)(j & 1), kWaitNs)) *flag = 1;
     tc_fence_after();
-    float d[16], d2[16];
+    float d[16], d2[16], d3[16], d4[16];
     tmem_ld16(tmem + lane_base + L::cD + 16 * hf, d);
     tmem_ld16(tmem + lane_base + L::cD + 32 + 16 * hf, d2);
+    tmem_ld16(tmem + lane_base + L::cD + 64 + 16 * hf, d3);
+    tmem_ld16(tmem + lane_base + L::cD + 96 + 16 * hf, d4);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] += d2[i] + lr[i];
+    for (int i = 0; i < 16; ++i) d[i] += ((d2[i] + d3[i]) + d4[i]) + lr[i];
     if (j + 1 == p.K) {
       float* dst = p.S_out + hoff + (size_t)(row0 + 16 * hf) * CTD + m;
 #pragma unroll
@@ -179,7 +200,7 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     tc_fence_before();
     __syncthreads();
     if (*flag) break;  // a wait gave up: issue nothing more (every thread reads the flag here)
-    if (tid == 0 || tid == 32) issue();
+    if (issuer) issue();
   }
 
   tc_fence_before();
