@@ -247,11 +247,21 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
           const int t = row;
           float av[32];
           if (fact[sl]) {
+            // (at Fc_s) kq in packed pairs; the 32x32 block of this warp's rows and columns is
+            // below, on or above the diagonal as a whole (warp-uniform), masked only on it
+            const int rel = quad - half;
             const float at = Fa_[t];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = half * 32 + i;
-              av[i] = s < t ? at * Fc_[s] * kq[i] : 0.f;
+            for (int i = 0; i < 32; i += 2) {
+              const float2 f = *reinterpret_cast<const float2*>(Fc_ + half * 32 + i);
+              const float2 x = __fmul2_rn(__fmul2_rn(make_float2(at, at), f), make_float2(kq[i], kq[i + 1]));
+              av[i] = rel < 0 ? 0.f : x.x;
+              av[i + 1] = rel < 0 ? 0.f : x.y;
+            }
+            if (rel == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (half * 32 + i >= t) av[i] = 0.f;
             }
           } else {
             const float bt = B_[t] * cRk[t], g_t = G2_[t];
@@ -271,11 +281,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
           unsigned char* Pst = sm + L::KQ + sl * 16384;
           float x[32];
           if (fact[sl]) {
+            const int rel = quad - 2 - half;
             const float at = Pa_[t];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = half * 32 + i;
-              x[i] = s <= t ? tf32r(at * Fc_[s] * kq[i]) : 0.f;
+            for (int i = 0; i < 32; i += 2) {
+              const float2 f = *reinterpret_cast<const float2*>(Fc_ + half * 32 + i);
+              const float2 y = __fmul2_rn(__fmul2_rn(make_float2(at, at), f), make_float2(kq[i], kq[i + 1]));
+              x[i] = rel < 0 ? 0.f : tf32r(y.x);
+              x[i + 1] = rel < 0 ? 0.f : tf32r(y.y);
+            }
+            if (rel == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (half * 32 + i > t) x[i] = 0.f;
             }
           } else {
             const float qt = cRq[t], g_t = G2_[t];
@@ -307,19 +325,21 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
       // record: Mb hi|lo, Mw, per-token factors
       const int h = hk * G + pair + slot;
       unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes;
-      // item (row t, columns [s, s + 8)): a quarter-warp writes whole 128-byte rows
+      // item (row t, columns [s, s + 8)): a quarter-warp writes whole 128-byte rows; the
+      // column factors are the same for all four rows of a thread
+      const int s = 8 * (gt & 7);
+      const float4 b0 = *reinterpret_cast<const float4*>(gB + s), b1 = *reinterpret_cast<const float4*>(gB + s + 4);
+      const float4 y0 = *reinterpret_cast<const float4*>(gGam + s), y1 = *reinterpret_cast<const float4*>(gGam + s + 4);
+      const float4 r0 = *reinterpret_cast<const float4*>(cRk + s), r1 = *reinterpret_cast<const float4*>(cRk + s + 4);
+      const float wf[8] = {y0.x * r0.x, y0.y * r0.y, y0.z * r0.z, y0.w * r0.w,
+                           y1.x * r1.x, y1.y * r1.y, y1.z * r1.z, y1.w * r1.w};
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
-        const int t = 16 * it + (gt >> 3), s = 8 * (gt & 7);
+        const int t = 16 * it + (gt >> 3);
         const float4 m0 = *reinterpret_cast<const float4*>(mmat + t * MST + s);
         const float4 m1 = *reinterpret_cast<const float4*>(mmat + t * MST + s + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(gB + s), b1 = *reinterpret_cast<const float4*>(gB + s + 4);
-        const float4 y0 = *reinterpret_cast<const float4*>(gGam + s), y1 = *reinterpret_cast<const float4*>(gGam + s + 4);
-        const float4 r0 = *reinterpret_cast<const float4*>(cRk + s), r1 = *reinterpret_cast<const float4*>(cRk + s + 4);
         const float mb[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
                              m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
-        const float wf[8] = {y0.x * r0.x, y0.y * r0.y, y0.z * r0.z, y0.w * r0.w,
-                             y1.x * r1.x, y1.y * r1.y, y1.z * r1.z, y1.w * r1.w};
         __align__(16) uint32_t bh[4], bl[4], wv[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
@@ -381,7 +401,7 @@ struct ScanLay {
   // while threads in different warps issue side by side; so each product is split by K over
   // ND1 / ND2 / NPU issuing warps, each into an accumulator of its own, and the epilogues add
   // the partial sums.  With 64-row slices the columns hold one accumulator per product.
-  static constexpr int ND1 = R == 32 ? 3 : 1, ND2 = R == 32 ? 2 : 1, NPU = R == 32 ? 2 : 1;
+  static constexpr int ND1 = R == 32 ? 2 : 1, ND2 = R == 32 ? 2 : 1, NPU = R == 32 ? 2 : 1;
   // accumulator a of [W;Q] S0^T for chunk parity b: cD1 + (2 a + b) R; of K^T U^ and P U: + a R
   static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = cD1 + 2 * R * ND1, cPU = cD2 + R * ND2;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -604,10 +624,9 @@ __global__ void __launch_bounds__(NT, 1)
         };
         if constexpr (L::ND1 == 1) {
           issue_range<0, 16>(d1);
-        } else {  // K steps 0-4, 5-9, 10-15
-          if (warp == 0) issue_range<0, 5>(d1);
-          else if (warp == 1) issue_range<5, 10>(d1);
-          else issue_range<10, 16>(d1);
+        } else {  // K steps 0-7, 8-15
+          if (warp == 0) issue_range<0, 8>(d1);
+          else issue_range<8, 16>(d1);
         }
         mma_commit(bar_d1);
       }
