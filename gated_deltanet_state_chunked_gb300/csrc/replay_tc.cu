@@ -414,6 +414,7 @@ struct ScanLay {
 
 struct ScanParams {
   const int32_t* cu;
+  const int32_t* order;  // tails longest first (scan CTA z takes tail order[z]), or null
   const float* S0;
   const unsigned char* rec;
   __nv_bfloat16* O;
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(NT, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3;
   const bool chain = warp < 4;
-  const int slice = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int slice = blockIdx.x, h = blockIdx.y, seq = p.order ? p.order[blockIdx.z] : (int)blockIdx.z;
   const int row0 = slice * R;
   const int hk = h / (p.h_v / p.h_k);
 
@@ -909,10 +910,34 @@ bool replay_tc_supported(const SimtParams& p) {
   return p.d_k == DK && p.d_v == DV && p.total_tokens > 0 && p.n_seqs > 0 && !p.augmented;
 }
 
-size_t replay_tc_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
+namespace {
+// Records of all chunks, then (several tails) the tail order.
+size_t records_bytes(int n_seqs, int total_tokens, int h_v) {
   // chunks of all tails <= ceil(total / 64) + one partial chunk per tail
   const size_t chunks = (size_t)(total_tokens + C - 1) / C + (size_t)n_seqs;
-  return chunks * (size_t)h_v * kRecBytes;
+  return (chunks * (size_t)h_v * kRecBytes + 255) / 256 * 256;
+}
+
+// Varlen work order: the tails ranked by length, longest first (ties by index), order[rank] =
+// tail.  The scan's grid walks the tails in this order, so the longest replays start in the
+// first wave and the last wave holds short ones (longest-processing-time-first list
+// scheduling: the grid's makespan is then bounded by the average load plus a short tail
+// rather than plus the longest one).  One thread per tail counts the tails ahead of it.
+__global__ void tail_order_kernel(const int32_t* __restrict__ cu, int n, int32_t* __restrict__ order) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const long long li = (long long)cu[i + 1] - cu[i];
+  int rank = 0;
+  for (int j = 0; j < n; ++j) {
+    const long long lj = (long long)cu[j + 1] - cu[j];
+    rank += (lj > li) || (lj == li && j < i);
+  }
+  order[rank] = i;
+}
+}  // namespace
+
+size_t replay_tc_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
+  return records_bytes(n_seqs, total_tokens, h_v) + (n_seqs > 1 ? (size_t)n_seqs * sizeof(int32_t) : 0);
 }
 
 cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -924,6 +949,13 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
       !make_map(&mv, p.v, p.total_tokens, (uint64_t)p.h_v * DV))
     return cudaErrorInvalidValue;
   unsigned char* rec = static_cast<unsigned char*>(workspace);
+  int32_t* order = nullptr;
+  if (p.n_seqs > 1) {  // several tails: longest first
+    order = reinterpret_cast<int32_t*>(rec + records_bytes(p.n_seqs, p.total_tokens, p.h_v));
+    tail_order_kernel<<<(p.n_seqs + 255) / 256, 256, 0, stream>>>(p.cu, p.n_seqs, order);
+    const cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+  }
 
   PrepParams pp;
   pp.g = p.g; pp.beta = p.beta; pp.cu = p.cu; pp.rec = rec; pp.status = p.status;
@@ -943,7 +975,7 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   }
 
   ScanParams sp;
-  sp.cu = p.cu; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
+  sp.cu = p.cu; sp.order = order; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
   sp.status = p.status; sp.n_seqs = p.n_seqs; sp.total_tokens = p.total_tokens; sp.h_k = p.h_k; sp.h_v = p.h_v;
   sp.write_O = p.write_O;
   return replay_tc_rows(p.n_seqs, p.h_v) == 64 ? launch_scan<64>(mq, mk, mv, sp, overlap, stream)
