@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "tc_common.cuh"
@@ -106,27 +107,55 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
   int* scratch = reinterpret_cast<int*>(sm + L::BARS + 32);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, half = warp >> 2;
-  const int gc = blockIdx.x, hk = blockIdx.y;
-  grid_dep_launch();  // the scan may start launching once every prep CTA is running
-  const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, -1, gc, scratch);
-  if (gc >= ci.total || ci.gc_seq < 0) return;
-  const int t0 = p.cu[ci.gc_seq] + ci.gc_idx * C;
-  const int n = min(C, p.cu[ci.gc_seq + 1] - t0);
   const int G = p.h_v / p.h_k;
-  // g and beta of the first slot pair, fetched now so that their latency overlaps the loads
-  // and the Gram below (warp 0 of each warpgroup: tokens lane and lane + 32 of its slot)
-  float pre[4] = {0.f, 0.f, 0.f, 0.f};
-  if ((warp & 3) == 0 && half < min(2, G)) {
-    const int h = hk * G + half;
-    if (lane < n) {
-      pre[0] = p.g[(size_t)(t0 + lane) * p.h_v + h];
-      pre[2] = p.beta[(size_t)(t0 + lane) * p.h_v + h];
+  grid_dep_launch();  // the scan may start launching once every prep CTA is running
+  // Work items (chunk, key head), item = chunk * h_k + key head, strided over a grid of about
+  // two CTAs per SM.  While a CTA works on one item it fetches the next one's gates and, once
+  // this item's P has left the [K;Q] area, its K and Q tiles.
+  struct Item {
+    int gc, hk, t0, n;
+    bool ok;
+  };
+  int total = 0;
+  auto item_at = [&](int item) {  // block-wide (chunk_info synchronises the CTA)
+    Item r;
+    r.gc = item / p.h_k;
+    r.hk = item - r.gc * p.h_k;
+    const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, -1, r.gc, scratch);
+    total = ci.total;
+    r.ok = r.gc < ci.total && ci.gc_seq >= 0;
+    r.t0 = r.ok ? p.cu[ci.gc_seq] + ci.gc_idx * C : 0;
+    r.n = r.ok ? min(C, p.cu[ci.gc_seq + 1] - r.t0) : 0;
+    return r;
+  };
+  // g and beta of an item's first slot pair (warp 0 of each warpgroup: tokens lane and lane + 32
+  // of its slot)
+  auto load_gb = [&](const Item& it, float (&pre)[4]) {
+    pre[0] = pre[1] = pre[2] = pre[3] = 0.f;
+    if (it.ok && (warp & 3) == 0 && half < min(2, G)) {
+      const int h = it.hk * G + half;
+      if (lane < it.n) {
+        pre[0] = p.g[(size_t)(it.t0 + lane) * p.h_v + h];
+        pre[2] = p.beta[(size_t)(it.t0 + lane) * p.h_v + h];
+      }
+      if (lane + 32 < it.n) {
+        pre[1] = p.g[(size_t)(it.t0 + lane + 32) * p.h_v + h];
+        pre[3] = p.beta[(size_t)(it.t0 + lane + 32) * p.h_v + h];
+      }
     }
-    if (lane + 32 < n) {
-      pre[1] = p.g[(size_t)(t0 + lane + 32) * p.h_v + h];
-      pre[3] = p.beta[(size_t)(t0 + lane + 32) * p.h_v + h];
+  };
+  auto issue_tma = [&](const Item& it) {  // one thread
+    mbar_arrive_expect_tx(bar_tma, 32768);
+    for (int a = 0; a < 2; ++a) {
+      tma_load_2d(sm + L::KQ + a * 16384, &map_k, bar_tma, it.hk * DK + a * 64, it.t0);
+      tma_load_2d(sm + L::KQ + a * 16384 + 8192, &map_q, bar_tma, it.hk * DK + a * 64, it.t0);
     }
-  }
+  };
+  Item cur = item_at(blockIdx.x);
+  const int n_items = total * p.h_k;
+  if ((int)blockIdx.x >= n_items) return;
+  float pre[4];
+  load_gb(cur, pre);
 
   if (warp == 0) {
     tmem_alloc(tmem_slot, 64);
@@ -136,11 +165,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
     mbar_fence_init();
-    mbar_arrive_expect_tx(bar_tma, 32768);
-    for (int a = 0; a < 2; ++a) {
-      tma_load_2d(sm + L::KQ + a * 16384, &map_k, bar_tma, hk * DK + a * 64, t0);
-      tma_load_2d(sm + L::KQ + a * 16384 + 8192, &map_q, bar_tma, hk * DK + a * 64, t0);
-    }
+    if (cur.ok) issue_tma(cur);
   }
   tc_fence_before();
   __syncthreads();
@@ -169,200 +194,228 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     r.ba = ba; r.bb = bb;
     return r;
   };
-  GateSums gs0 = {};
-  if ((warp & 3) == 0 && half < min(2, G)) gs0 = gate_sums(pre[0], pre[1], pre[2], pre[3]);
-  bool ok = mbar_wait(bar_tma, 0, kWaitNs);
-  if (tid == 0) {
-    const uint64_t d = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);
-    constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+  int done = 0;  // items processed: the parity of bar_tma and bar_mma
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int gc = cur.gc, hk = cur.hk, t0 = cur.t0, n = cur.n;
+    Item nxt{0, 0, 0, 0, false};
+    if (item + (int)gridDim.x < n_items) nxt = item_at(item + gridDim.x);  // uniform
+    float pre_n[4];
+    load_gb(nxt, pre_n);  // in flight during this item
+    if (!cur.ok) {  // (not reached for well-formed offsets) nothing was fetched for this item
+      cur = nxt;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint64_t dj = d + (uint64_t)((((j >> 2) * 16384) + (j & 3) * 32) >> 4);
-      mma_bf16(tmem, dj, dj, id, j > 0);
+      for (int i = 0; i < 4; ++i) pre[i] = pre_n[i];
+      if (tid == 0 && cur.ok) issue_tma(cur);
+      continue;
     }
-    mma_commit(bar_mma);
-  }
-  {  // norms: 128 rows (64 keys, 64 queries) x 2 atoms, rotated chunk order (no bank conflicts)
-    const int row = tid >> 1, atom = tid & 1;
-    float ss = row_sumsq(sm + L::KQ + atom * 16384 + row * 128, row);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    if (atom == 0) {
-      const float r = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
-      if (row < 64) cRk[row] = r;
-      else cRq[row - 64] = r * p.scale;
-    }
-  }
-  ok = mbar_wait(bar_mma, 0, kWaitNs) && ok;
-  tc_fence_after();
-  float kq[32];  // row (32*quad + lane) of [K;Q] K^T, columns [32*half, +32)
-  tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + half * 32, kq);
-  tmem_ld_wait();
-  if (!ok && tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
-  __syncthreads();
-
-  const int slot = half, gt = tid & 127;  // warpgroup = v-head slot
-  unsigned char* sslot = sm + L::SLOT + slot * L::SLOT_BYTES;
-  float* amat = reinterpret_cast<float*>(sslot + L::AMAT);
-  float* mmat = reinterpret_cast<float*>(sslot + L::MMAT);
-  float* gB = reinterpret_cast<float*>(sslot + L::GATE);  // beta
-  float* gG2 = gB + 64;   // G log2(e)
-  float* gFa = gB + 128;  // beta_t rk_t exp2(G_t - G_last)
-  float* gFc = gB + 192;  // rk_s exp2(G_last - G_s)
-  float* gPa = gB + 256;  // rq_t exp2(G_t - G_last)
-  float* gGam = gB + 320; // gamma_t
-
-  for (int pair = 0; pair < G; pair += 2) {
-    const int nslots = min(2, G - pair);
-    // gates of both slots: warp 0 of each warpgroup
-    if ((warp & 3) == 0 && slot < nslots) {
-      const int h = hk * G + pair + slot;
-      GateSums q = gs0;
-      if (pair > 0) {
-        const float ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-        const float gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
-        const float ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
-        const float bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
-        q = gate_sums(ga, gb, ba, bb);
+    const uint32_t ph = (uint32_t)(done & 1);
+    GateSums gs0 = {};
+    if ((warp & 3) == 0 && half < min(2, G)) gs0 = gate_sums(pre[0], pre[1], pre[2], pre[3]);
+    bool ok = mbar_wait(bar_tma, ph, kWaitNs);
+    if (tid == 0) {
+      tc_fence_after();  // the previous item's Gram has been read out of TMEM by every thread
+      const uint64_t d = sdesc_sw128(smem_u32(sm + L::KQ), 16, 1024);
+      constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint64_t dj = d + (uint64_t)((((j >> 2) * 16384) + (j & 3) * 32) >> 4);
+        mma_bf16(tmem, dj, dj, id, j > 0);
       }
-      const float la = q.la, lb = q.lb, ea = q.ea, eb = q.eb, fa = q.fa, fb = q.fb, ba = q.ba, bb = q.bb;
-      const float last = __shfl_sync(0xffffffffu, lb, 31);
-      gB[lane] = ba; gB[lane + 32] = bb;
-      gG2[lane] = la; gG2[lane + 32] = lb;
-      gFa[lane] = ba * cRk[lane] * ea; gFa[lane + 32] = bb * cRk[lane + 32] * eb;
-      gFc[lane] = cRk[lane] * fa; gFc[lane + 32] = cRk[lane + 32] * fb;
-      gPa[lane] = cRq[lane] * ea; gPa[lane + 32] = cRq[lane + 32] * eb;
-      gGam[lane] = exp2f(la); gGam[lane + 32] = exp2f(lb);
-      if (lane == 0) fact[slot] = (la - last) < kFactorRange ? 1 : 0;
+      mma_commit(bar_mma);
     }
+    {  // norms: 128 rows (64 keys, 64 queries) x 2 atoms, rotated chunk order (no bank conflicts)
+      const int row = tid >> 1, atom = tid & 1;
+      float ss = row_sumsq(sm + L::KQ + atom * 16384 + row * 128, row);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (atom == 0) {
+        const float r = p.l2norm ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
+        if (row < 64) cRk[row] = r;
+        else cRq[row - 64] = r * p.scale;
+      }
+    }
+    ok = mbar_wait(bar_mma, ph, kWaitNs) && ok;
+    tc_fence_after();
+    float kq[32];  // row (32*quad + lane) of [K;Q] K^T, columns [32*half, +32)
+    tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + half * 32, kq);
+    tmem_ld_wait();
+    tc_fence_before();
+    if (!ok && tid == 0) atomicExch(p.status, GDN_ERR_TIMEOUT);
     __syncthreads();
-    // A (key rows) and P (query rows) for each slot from this thread's Gram row
-    {
-      const int row = 32 * quad + lane;
-      for (int sl = 0; sl < nslots; ++sl) {
-        unsigned char* ss_ = sm + L::SLOT + sl * L::SLOT_BYTES;
-        float* A_ = reinterpret_cast<float*>(ss_ + L::AMAT);
-        const float* B_ = reinterpret_cast<const float*>(ss_ + L::GATE);
-        const float *G2_ = B_ + 64, *Fa_ = B_ + 128, *Fc_ = B_ + 192, *Pa_ = B_ + 256;
-        if (row < 64) {
-          const int t = row;
-          float av[32];
-          if (fact[sl]) {
-            // (at Fc_s) kq in packed pairs; the 32x32 block of this warp's rows and columns is
-            // below, on or above the diagonal as a whole (warp-uniform), masked only on it
-            const int rel = quad - half;
-            const float at = Fa_[t];
+
+    const int slot = half, gt = tid & 127;  // warpgroup = v-head slot
+    unsigned char* sslot = sm + L::SLOT + slot * L::SLOT_BYTES;
+    float* amat = reinterpret_cast<float*>(sslot + L::AMAT);
+    float* mmat = reinterpret_cast<float*>(sslot + L::MMAT);
+    float* gB = reinterpret_cast<float*>(sslot + L::GATE);  // beta
+    float* gG2 = gB + 64;   // G log2(e)
+    float* gFa = gB + 128;  // beta_t rk_t exp2(G_t - G_last)
+    float* gFc = gB + 192;  // rk_s exp2(G_last - G_s)
+    float* gPa = gB + 256;  // rq_t exp2(G_t - G_last)
+    float* gGam = gB + 320; // gamma_t
+
+    for (int pair = 0; pair < G; pair += 2) {
+      const int nslots = min(2, G - pair);
+      // gates of both slots: warp 0 of each warpgroup
+      if ((warp & 3) == 0 && slot < nslots) {
+        const int h = hk * G + pair + slot;
+        GateSums q = gs0;
+        if (pair > 0) {
+          const float ga = lane < n ? p.g[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+          const float gb = lane + 32 < n ? p.g[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+          const float ba = lane < n ? p.beta[(size_t)(t0 + lane) * p.h_v + h] : 0.f;
+          const float bb = lane + 32 < n ? p.beta[(size_t)(t0 + lane + 32) * p.h_v + h] : 0.f;
+          q = gate_sums(ga, gb, ba, bb);
+        }
+        const float la = q.la, lb = q.lb, ea = q.ea, eb = q.eb, fa = q.fa, fb = q.fb, ba = q.ba, bb = q.bb;
+        const float last = __shfl_sync(0xffffffffu, lb, 31);
+        gB[lane] = ba; gB[lane + 32] = bb;
+        gG2[lane] = la; gG2[lane + 32] = lb;
+        gFa[lane] = ba * cRk[lane] * ea; gFa[lane + 32] = bb * cRk[lane + 32] * eb;
+        gFc[lane] = cRk[lane] * fa; gFc[lane + 32] = cRk[lane + 32] * fb;
+        gPa[lane] = cRq[lane] * ea; gPa[lane + 32] = cRq[lane + 32] * eb;
+        gGam[lane] = exp2f(la); gGam[lane + 32] = exp2f(lb);
+        if (lane == 0) fact[slot] = (la - last) < kFactorRange ? 1 : 0;
+      }
+      __syncthreads();
+      // A (key rows) and P (query rows) for each slot from this thread's Gram row
+      {
+        const int row = 32 * quad + lane;
+        for (int sl = 0; sl < nslots; ++sl) {
+          unsigned char* ss_ = sm + L::SLOT + sl * L::SLOT_BYTES;
+          float* A_ = reinterpret_cast<float*>(ss_ + L::AMAT);
+          const float* B_ = reinterpret_cast<const float*>(ss_ + L::GATE);
+          const float *G2_ = B_ + 64, *Fa_ = B_ + 128, *Fc_ = B_ + 192, *Pa_ = B_ + 256;
+          if (row < 64) {
+            const int t = row;
+            float av[32];
+            if (fact[sl]) {
+              // (at Fc_s) kq in packed pairs; the 32x32 block of this warp's rows and columns is
+              // below, on or above the diagonal as a whole (warp-uniform), masked only on it
+              const int rel = quad - half;
+              const float at = Fa_[t];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 f = *reinterpret_cast<const float2*>(Fc_ + half * 32 + i);
-              const float2 x = __fmul2_rn(__fmul2_rn(make_float2(at, at), f), make_float2(kq[i], kq[i + 1]));
-              av[i] = rel < 0 ? 0.f : x.x;
-              av[i + 1] = rel < 0 ? 0.f : x.y;
-            }
-            if (rel == 0) {
+              for (int i = 0; i < 32; i += 2) {
+                const float2 f = *reinterpret_cast<const float2*>(Fc_ + half * 32 + i);
+                const float2 x = __fmul2_rn(__fmul2_rn(make_float2(at, at), f), make_float2(kq[i], kq[i + 1]));
+                av[i] = rel < 0 ? 0.f : x.x;
+                av[i + 1] = rel < 0 ? 0.f : x.y;
+              }
+              if (rel == 0) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (half * 32 + i >= t) av[i] = 0.f;
-            }
-          } else {
-            const float bt = B_[t] * cRk[t], g_t = G2_[t];
+                for (int i = 0; i < 32; ++i)
+                  if (half * 32 + i >= t) av[i] = 0.f;
+              }
+            } else {
+              const float bt = B_[t] * cRk[t], g_t = G2_[t];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = half * 32 + i;
-              av[i] = s < t ? bt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i] : 0.f;
+              for (int i = 0; i < 32; ++i) {
+                const int s = half * 32 + i;
+                av[i] = s < t ? bt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i] : 0.f;
+              }
             }
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(A_ + t * MST + half * 32 + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
+          } else if (p.write_O) {
+            const int t = row - 64;
+            // staged in the record's own layout in the [K;Q] area (free once the Gram and the norms
+            // have read it), 16 KB per slot, then stored by one bulk copy
+            unsigned char* Pst = sm + L::KQ + sl * 16384;
+            float x[32];
+            if (fact[sl]) {
+              const int rel = quad - 2 - half;
+              const float at = Pa_[t];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 f = *reinterpret_cast<const float2*>(Fc_ + half * 32 + i);
+                const float2 y = __fmul2_rn(__fmul2_rn(make_float2(at, at), f), make_float2(kq[i], kq[i + 1]));
+                x[i] = rel < 0 ? 0.f : tf32r(y.x);
+                x[i + 1] = rel < 0 ? 0.f : tf32r(y.y);
+              }
+              if (rel == 0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (half * 32 + i > t) x[i] = 0.f;
+              }
+            } else {
+              const float qt = cRq[t], g_t = G2_[t];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int s = half * 32 + i;
+                x[i] = s <= t ? tf32r(qt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i]) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(Pst + kf32(t, half * 32 + i, 64)) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
           }
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(A_ + t * MST + half * 32 + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
-        } else if (p.write_O) {
-          const int t = row - 64;
-          // staged in the record's own layout in the [K;Q] area (free once the Gram and the norms
-          // have read it), 16 KB per slot, then stored by one bulk copy
-          unsigned char* Pst = sm + L::KQ + sl * 16384;
-          float x[32];
-          if (fact[sl]) {
-            const int rel = quad - 2 - half;
-            const float at = Pa_[t];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 f = *reinterpret_cast<const float2*>(Fc_ + half * 32 + i);
-              const float2 y = __fmul2_rn(__fmul2_rn(make_float2(at, at), f), make_float2(kq[i], kq[i + 1]));
-              x[i] = rel < 0 ? 0.f : tf32r(y.x);
-              x[i + 1] = rel < 0 ? 0.f : tf32r(y.y);
-            }
-            if (rel == 0) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (half * 32 + i > t) x[i] = 0.f;
-            }
-          } else {
-            const float qt = cRq[t], g_t = G2_[t];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = half * 32 + i;
-              x[i] = s <= t ? tf32r(qt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i]) : 0.f;
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(Pst + kf32(t, half * 32 + i, 64)) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
         }
       }
-    }
-    fence_async_smem();  // the staged P -> the bulk copy
-    __syncthreads();
-    // P to the record: one 16 KB bulk copy, in flight during the inverse.  Issued by a thread of
-    // warp 3 of the slot, which only clears M's upper blocks before the inverse's first barrier
-    // (issuing can hold a thread for about a thousand cycles).
-    const bool issP = p.write_O && slot < nslots && gt == 96;
-    if (issP) {
-      const int h = hk * G + pair + slot;
-      bulk_store(p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP, sm + L::KQ + slot * 16384, 16384);
-      bulk_commit();
-    }
-    if (slot < nslots) {
-      invert_unit_lower(amat, mmat, gt, 1 + slot);
-      // record: Mb hi|lo, Mw, per-token factors
-      const int h = hk * G + pair + slot;
-      unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes;
-      // item (row t, columns [s, s + 8)): a quarter-warp writes whole 128-byte rows; the
-      // column factors are the same for all four rows of a thread
-      const int s = 8 * (gt & 7);
-      const float4 b0 = *reinterpret_cast<const float4*>(gB + s), b1 = *reinterpret_cast<const float4*>(gB + s + 4);
-      const float4 y0 = *reinterpret_cast<const float4*>(gGam + s), y1 = *reinterpret_cast<const float4*>(gGam + s + 4);
-      const float4 r0 = *reinterpret_cast<const float4*>(cRk + s), r1 = *reinterpret_cast<const float4*>(cRk + s + 4);
-      const float wf[8] = {y0.x * r0.x, y0.y * r0.y, y0.z * r0.z, y0.w * r0.w,
-                           y1.x * r1.x, y1.y * r1.y, y1.z * r1.z, y1.w * r1.w};
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int t = 16 * it + (gt >> 3);
-        const float4 m0 = *reinterpret_cast<const float4*>(mmat + t * MST + s);
-        const float4 m1 = *reinterpret_cast<const float4*>(mmat + t * MST + s + 4);
-        const float mb[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
-                             m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
-        __align__(16) uint32_t bh[4], bl[4], wv[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          // Mb as bf16 hi + lo, both truncated (|error| < 2^-16 |Mb|); Mw rounded to nearest even
-          const float h0 = __uint_as_float(__float_as_uint(mb[e]) & 0xffff0000u);
-          const float h1 = __uint_as_float(__float_as_uint(mb[e + 1]) & 0xffff0000u);
-          bh[e / 2] = bf16x2_trunc(h0, h1);
-          bl[e / 2] = bf16x2_trunc(mb[e] - h0, mb[e + 1] - h1);
-          wv[e / 2] = bf16x2_rne(mb[e] * wf[e], mb[e + 1] * wf[e + 1]);
+      fence_async_smem();  // the staged P -> the bulk copy
+      __syncthreads();
+      // P to the records: a 16 KB bulk copy per slot, in flight during the inverse.  Issued by a
+      // thread of warp 3 of slot 0, which only clears M's upper blocks before the inverse's first
+      // barrier (issuing can hold a thread for about a thousand cycles).
+      const bool issP = p.write_O && tid == 96;
+      if (issP) {
+        for (int sl = 0; sl < nslots; ++sl) {
+          const int h = hk * G + pair + sl;
+          bulk_store(p.rec + ((size_t)gc * p.h_v + h) * kRecBytes + kRecP, sm + L::KQ + sl * 16384, 16384);
         }
-        *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(bh);
-        *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, 64 + s, 64)) = *reinterpret_cast<const uint4*>(bl);
-        *reinterpret_cast<uint4*>(rec + kRecMW + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(wv);
+        bulk_commit();
       }
-      if (gt < 64) {
-        float* gate = reinterpret_cast<float*>(rec + kRecGate);
-        gate[gt] = gGam[gt];
-        gate[64 + gt] = gFc[gt];
-        gate[128 + gt] = gGam[gt] * cRq[gt];
+      if (slot < nslots) {
+        invert_unit_lower(amat, mmat, gt, 1 + slot);
+        if (tid == 96 && pair + 2 >= G && nxt.ok) {  // the next item's K and Q tiles: the [K;Q]
+          if (p.write_O) bulk_wait_read_all();       // area is free once the P copies have read it
+          issue_tma(nxt);
+        }
+        // record: Mb hi|lo, Mw, per-token factors
+        const int h = hk * G + pair + slot;
+        unsigned char* rec = p.rec + ((size_t)gc * p.h_v + h) * kRecBytes;
+        // item (row t, columns [s, s + 8)): a quarter-warp writes whole 128-byte rows; the
+        // column factors are the same for all four rows of a thread
+        const int s = 8 * (gt & 7);
+        const float4 b0 = *reinterpret_cast<const float4*>(gB + s), b1 = *reinterpret_cast<const float4*>(gB + s + 4);
+        const float4 y0 = *reinterpret_cast<const float4*>(gGam + s), y1 = *reinterpret_cast<const float4*>(gGam + s + 4);
+        const float4 r0 = *reinterpret_cast<const float4*>(cRk + s), r1 = *reinterpret_cast<const float4*>(cRk + s + 4);
+        const float wf[8] = {y0.x * r0.x, y0.y * r0.y, y0.z * r0.z, y0.w * r0.w,
+                             y1.x * r1.x, y1.y * r1.y, y1.z * r1.z, y1.w * r1.w};
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int t = 16 * it + (gt >> 3);
+          const float4 m0 = *reinterpret_cast<const float4*>(mmat + t * MST + s);
+          const float4 m1 = *reinterpret_cast<const float4*>(mmat + t * MST + s + 4);
+          const float mb[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
+                               m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
+          __align__(16) uint32_t bh[4], bl[4], wv[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            // Mb as bf16 hi + lo, both truncated (|error| < 2^-16 |Mb|); Mw rounded to nearest even
+            const float h0 = __uint_as_float(__float_as_uint(mb[e]) & 0xffff0000u);
+            const float h1 = __uint_as_float(__float_as_uint(mb[e + 1]) & 0xffff0000u);
+            bh[e / 2] = bf16x2_trunc(h0, h1);
+            bl[e / 2] = bf16x2_trunc(mb[e] - h0, mb[e + 1] - h1);
+            wv[e / 2] = bf16x2_rne(mb[e] * wf[e], mb[e + 1] * wf[e + 1]);
+          }
+          *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(bh);
+          *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, 64 + s, 64)) = *reinterpret_cast<const uint4*>(bl);
+          *reinterpret_cast<uint4*>(rec + kRecMW + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(wv);
+        }
+        if (gt < 64) {
+          float* gate = reinterpret_cast<float*>(rec + kRecGate);
+          gate[gt] = gGam[gt];
+          gate[64 + gt] = gFc[gt];
+          gate[128 + gt] = gGam[gt] * cRq[gt];
+        }
       }
+      if (issP) bulk_wait_read_all();  // the next pair restages P; the source stays until read
+      __syncthreads();
     }
-    if (issP) bulk_wait_read_all();  // the next pair restages P; the source stays until read
-    __syncthreads();
+    ++done;
+    cur = nxt;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pre[i] = pre_n[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -963,8 +1016,13 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   pp.write_O = p.write_O; pp.scale = p.scale;
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepLay::ALLOC);
   if (e != cudaSuccess) return e;
-  const int chunks_ub = (p.total_tokens + C - 1) / C + p.n_seqs;
-  chunk_prep_kernel<<<dim3(chunks_ub, p.h_k), NT, PrepLay::ALLOC, stream>>>(mq, mk, pp);
+  const long long items_ub = ((long long)(p.total_tokens + C - 1) / C + p.n_seqs) * p.h_k;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  const int grid = (int)std::min<long long>(items_ub, 2LL * sms);  // two CTAs per SM
+  chunk_prep_kernel<<<grid, NT, PrepLay::ALLOC, stream>>>(mq, mk, pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bool overlap = true;  // a stage event between the kernels asks for them to run one after the other

@@ -73,6 +73,22 @@ def test_ragged_many_problems_64_row_slices():
     _check(x, O, S)
 
 
+def test_many_tails_each_replayed_once():
+    """300 tails (more than one block of the longest-first ordering), lengths out of order and
+    with ties, so that the scan's grid takes them in a permuted order: every tail's state must
+    match the oracle on its own (a tail skipped or taken twice would not)."""
+    rng = np.random.Generator(np.random.PCG64(310))
+    lengths = [int(v) for v in rng.integers(0, 140, size=290)] + [70] * 10
+    rng.shuffle(lengths)
+    x = synthetic.make_replay_inputs(lengths, 1, 2, 128, 128, dtype="bf16", seed=311, with_S0=True)
+    O, S = _run(x)
+    S_ref, O_ref = oracle_replay(x)
+    Sh = host(S)
+    worst = max(rel_err(Sh[i], S_ref[i]) for i in range(len(lengths)))
+    assert worst <= TOL_BF16, f"worst per-tail S rel err {worst:.3e}"
+    assert rel_err(host(O), O_ref) <= TOL_BF16
+
+
 def test_weak_decay_carry():
     """g scaled by 1e-3: the state entering each chunk dominates, so errors in the
     inter-chunk carry would show."""
