@@ -455,6 +455,7 @@ struct ScanLay {
   // ND1 / ND2 / NPU issuing warps, each into an accumulator of its own, and the epilogues add
   // the partial sums.  With 64-row slices the columns hold one accumulator per product.
   static constexpr int ND1 = R == 32 ? 2 : 1, ND2 = R == 32 ? 2 : 1, NPU = R == 32 ? 2 : 1;
+  static_assert(ND1 <= 2 && ND2 <= 2 && NPU <= 2, "the epilogues add at most two partial sums");
   // accumulator a of [W;Q] S0^T for chunk parity b: cD1 + (2 a + b) R; of K^T U^ and P U: + a R
   static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = cD1 + 2 * R * ND1, cPU = cD2 + R * ND2;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -691,17 +692,18 @@ __global__ void __launch_bounds__(NT, 1)
         const float sc = gate[64 + t];
 #pragma unroll
         for (int hh = 0; hh < R / 32; ++hh) {  // 32 state rows at a time
-          float ut[32], dw[32];
+          float ut[32], dw[32], x[32];
           tmem_ld32(tmem + lane_base + L::cU + par * R + 32 * hh, ut);
           tmem_ld32(tmem + lane_base + L::cD1 + par * R + 32 * hh, dw);
+          if constexpr (L::ND1 == 2) tmem_ld32(tmem + lane_base + L::cD1 + (2 + par) * R + 32 * hh, x);
           tmem_ld_wait();
+          if constexpr (L::ND1 == 2) {
 #pragma unroll
-          for (int a = 1; a < L::ND1; ++a) {
-            float x[32];
-            tmem_ld32(tmem + lane_base + L::cD1 + (2 * a + par) * R + 32 * hh, x);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dw[i] += x[i];
+            for (int i = 0; i < 32; i += 2) {
+              const float2 w = __fadd2_rn(make_float2(dw[i], dw[i + 1]), make_float2(x[i], x[i + 1]));
+              dw[i] = w.x;
+              dw[i + 1] = w.y;
+            }
           }
           // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
           __align__(16) uint32_t hp[16], lp[16];
@@ -773,22 +775,20 @@ __global__ void __launch_bounds__(NT, 1)
         const float gC = gate[63];
 #pragma unroll
         for (int hh = 0; hh < R / 32; ++hh) {
-          float d2[32];
+          float d2[32], x[32];
           tmem_ld32(tmem + lane_base + L::cD2 + 32 * hh, d2);
+          if constexpr (L::ND2 == 2) tmem_ld32(tmem + lane_base + L::cD2 + R + 32 * hh, x);
           tmem_ld_wait();
 #pragma unroll
-          for (int a = 1; a < L::ND2; ++a) {
-            float x[32];
-            tmem_ld32(tmem + lane_base + L::cD2 + a * R + 32 * hh, x);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) d2[i] += x[i];
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 32; i += 2) {  // packed pairs (same rounding as the scalar forms)
             const int r = 32 * hh + i;
-            sreg[r] = fmaf(gC, sreg[r], d2[i]);
-            *reinterpret_cast<float*>(sm + L::S32 + kf32(r, dcol, R)) = tf32r(sreg[r]);
+            float2 d = make_float2(d2[i], d2[i + 1]);
+            if constexpr (L::ND2 == 2) d = __fadd2_rn(d, make_float2(x[i], x[i + 1]));
+            const float2 sn = __ffma2_rn(make_float2(gC, gC), make_float2(sreg[r], sreg[r + 1]), d);
+            sreg[r] = sn.x;
+            sreg[r + 1] = sn.y;
+            *reinterpret_cast<float*>(sm + L::S32 + kf32(r, dcol, R)) = tf32r(sn.x);
+            *reinterpret_cast<float*>(sm + L::S32 + kf32(r + 1, dcol, R)) = tf32r(sn.y);
           }
         }
       }
