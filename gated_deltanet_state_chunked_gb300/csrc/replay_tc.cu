@@ -11,11 +11,13 @@
 //   S    = gamma_C S0 + K^T diag(rk exp(G_C - G_s)) U     (carried in fp32)
 //   O    = diag(gamma) Q^ S0^T + P U,   P_ts = exp(G_t - G_s) q^_t.k^_s (s <= t)
 //
-// Two kernels:
-//  * chunk_prep_kernel -- one CTA per (chunk, key head), all chunks of all tails
-//    in parallel: K K^T on tcgen05, the gated A, and M = (I + A)^{-1} on CUDA
-//    cores (32x32 diagonal blocks by forward substitution, then one block merge), written
-//    with beta, G and rk to a per-(chunk, v-head) record in scratch memory.
+// Kernels:
+//  * chunk_prep_kernel -- the (chunk, key head) items of all tails, walked by a persistent
+//    grid of two CTAs per SM: K K^T on tcgen05, the gated A and P, and M = (I + A)^{-1}
+//    (16x16 diagonal blocks by forward substitution on CUDA cores, then two levels of block
+//    merges on warp-level tensor cores), written with beta, G and rk to a per-(chunk, v-head)
+//    record in scratch memory.
+//  * tail_order_kernel -- with several tails, their order longest first.
 //  * chunk_scan_kernel -- one CTA per 32- or 64-row slice of d_v of one (tail, v-head)
 //    state, walking the tail's chunks (R = 32 while all slices fit on the GPU at once, else
 //    64).  Per chunk:
