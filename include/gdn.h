@@ -92,7 +92,9 @@ typedef struct {
  *                Rows outside every sequence's range are not written.
  *   S_out        fp32 [n_seqs][h_v][d_v][d_k]; may alias S0 (in-place update)
  * Computation: chunks of 64 tokens, fp32 state carried between chunks.  bf16
- * inputs with 128-dim heads run on the tcgen05 tensor cores.  fp32 inputs,
+ * inputs with 128-dim heads run on the tcgen05 tensor cores; with several tails
+ * their sequential scans start longest first (a small kernel ranks the tails by
+ * length on the stream before the chunk kernels).  fp32 inputs,
  * other head sizes and GDN_PRECISE take the fp32 path: fp32 data, its
  * contractions in split tf32 on warp-level tensor cores (about 21 significant
  * bits), in two passes with pool scratch of (ceil(total_tokens / 64) + n_seqs)
