@@ -89,6 +89,16 @@ def test_many_tails_each_replayed_once():
     assert rel_err(host(O), O_ref) <= TOL_BF16
 
 
+@pytest.mark.parametrize("h_k,h_v", [(1, 4), (1, 3)])
+def test_more_than_two_v_heads_per_key_head(h_k, h_v):
+    """Four and three v-heads per key head: the prep kernel treats a key head's v-heads in
+    pairs, so these take its second pass (and an odd last pair)."""
+    x = synthetic.make_replay_inputs([130, 64, 5], h_k, h_v, 128, 128, dtype="bf16", seed=320 + h_v,
+                                     with_S0=True)
+    O, S = _run(x)
+    _check(x, O, S)
+
+
 def test_weak_decay_carry():
     """g scaled by 1e-3: the state entering each chunk dominates, so errors in the
     inter-chunk carry would show."""
