@@ -132,10 +132,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
-}
-
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   K-major operand:  rows (M or N) of 128 B, 8-row groups 1024 B apart (SBO);
@@ -204,8 +200,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 // Shared -> global bulk copy (both addresses 16-byte aligned, bytes a multiple of 16), tracked
-// by the issuing thread's bulk groups: commit after issuing, then wait before the source is
-// rewritten (.read: the source has been read) or before the thread exits (all writes done).
+// by the issuing thread's bulk groups: commit after issuing, then wait until the source has
+// been read before it is rewritten or the CTA exits.
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
                "r"(smem_u32(ssrc)), "r"(bytes)
@@ -213,14 +209,8 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// Byte offset of element (row r, 16-byte chunk c) inside a 128 B-swizzled tile whose rows are 128 B.
-__host__ __device__ constexpr uint32_t sw128_offset(uint32_t r, uint32_t chunk) {
-  return r * 128u + ((chunk ^ (r & 7u)) << 4);
 }
 
 }  // namespace tc
