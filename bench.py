@@ -115,6 +115,16 @@ def recorded_traffic(workload: str):
     return None
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value over all ranks (the slowest rank's time); x itself on one rank."""
+    if dist is None or not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -414,10 +424,7 @@ def run_ours(args):
         stages = {"chunk_prep_kernel_us": prep_ms * 1e3, "chunk_scan_kernel_us": scan_ms * 1e3,
                   "dominant": "chunk_scan_kernel" if scan_ms >= prep_ms else "chunk_prep_kernel",
                   "measured": f"{ks} separate calls with the kernels serialised by a stage event"}
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # parity of the last timed step on a few sampled (tail, head) problems
     import oracle
@@ -499,10 +506,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         e2e_ms = e2e_run(args.steps) / args.steps
         api.gdn_get_status()
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "pipelining": f"{NB} streams, {NB} buffer sets: uploads of later steps overlap a step's replay and read-back; one copy per direction per step"}
@@ -542,7 +546,8 @@ def run_ours(args):
         "config": describe(args.workload, x) | {"path": "precise" if args.precise else "default",
                                                 "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": args.steps * (2 if tensor_path else 1),
+        # per call: the two chunk kernels, plus the tail-order kernel when several tails share a call
+        "gpu_launches": args.steps * (2 + (1 if tensor_path and x.n_seqs > 1 else 0)),
         "clocks": clocks, "parity": parity, "rows": rows,
     }
     print(json.dumps(line), flush=True)
