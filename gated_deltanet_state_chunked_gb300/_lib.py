@@ -66,6 +66,7 @@ SIGNATURES = {
     "gdn_workspace_bytes": ([_PD], ctypes.c_size_t),
     "gdn_abi_version": ([], ctypes.c_int),
     "gdn_set_stage_event": ([_VP], None),
+    "gdn_set_wait_limit_ns": ([ctypes.c_uint64], None),
 }
 
 

@@ -196,3 +196,9 @@ def gdn_set_stage_event(event) -> None:
     if event is not None and event.cuda_event == 0:
         raise ValueError("record-able torch.cuda.Event expected")
     lib.gdn_set_stage_event(ctypes.c_void_p(event.cuda_event if event is not None else 0))
+
+
+def gdn_set_wait_limit_ns(ns: int) -> None:
+    """Bound of the device-side waits of this thread's next gdn_compose call (test hook of the
+    timeout path; 0 makes a wait give up unless its event has already happened)."""
+    _lib.load().gdn_set_wait_limit_ns(int(ns))

@@ -1,7 +1,8 @@
 // Tensor-core composition of chunk operators for d_k = d_v = 128.
 //
-// Method: "LinearKV" section 3 and "HYPIC" section 3.2 (chunk operators): the state after K
-// chunks is S_K = T_K ... T_1 S_in + sum_j T_K ... T_{j+1} S_local_j in the pages' left form,
+// Method: "LinearKV: One Cached State Suffices for Position-Independent Caching in Hybrid
+// LLMs", composition passage (affine chunk operators, exact closed-form composition): the state
+// after K chunks is S_K = T_K ... T_1 S_in + sum_j T_K ... T_{j+1} S_local_j in the pages' left form,
 // which in the row-major convention of this library (S_out = S_in T^T + S_local) is the Horner
 // recursion S_j = S_{j-1} T_j^T + S_local_j, j = 1..K.
 //
@@ -165,12 +166,13 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
   tc_fence_before();
   __syncthreads();
   if (issuer) issue();
+  int issued = 0;  // the last step whose MMAs were issued
   if (p.K > 1) fetch_T(1);
   fetch_L(0);
 
   for (int j = 0; j < p.K; ++j) {
     // step j's MMAs done: S_j = D + S_local_j
-    if (!mbar_wait(bar, (uint32_t)(j & 1), kWaitNs)) *flag = 1;
+    if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) *flag = 1;
     tc_fence_after();
     float d[16], d2[16], d3[16], d4[16];
     tmem_ld16(tmem + lane_base + L::cD + 16 * hf, d);
@@ -201,11 +203,22 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     __syncthreads();
     if (*flag) break;  // a wait gave up: issue nothing more (every thread reads the flag here)
     if (issuer) issue();
+    issued = j + 1;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *flag) atomicExch(p.status, GDN_ERR_TIMEOUT);
+  if (*flag) {
+    // A wait gave up: the MMAs already issued still write TMEM, so let them finish (their last
+    // step's phase, at the default bound) before the columns are released, then report.
+    if (tid == 0) {
+      mbar_wait(bar, (uint32_t)(issued & 1), kWaitNs);
+      atomicExch(p.status, GDN_ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 

@@ -14,6 +14,8 @@ namespace {
 
 thread_local std::string g_last_error;
 thread_local void* g_stage_event = nullptr;  // cudaEvent_t to record between prep and scan, once
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+thread_local unsigned long long g_wait_ns = kDefaultWaitNs;  // next compose call's wait limit, once
 
 int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int code, const char* fmt, ...) {
@@ -76,8 +78,8 @@ int scratch_pool(cudaMemPool_t* out) {
 
 }  // namespace
 
-// Argument checks of the allocation-free replay entry point (same rules as
-// gdn_replay): fills *p, sets *nothing_to_do for an empty batch.
+// Argument checks of gdn_replay and gdn_replay_noalloc (one set of rules for both): fills *p,
+// sets *nothing_to_do for an empty batch.
 int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
                       const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
                       SimtParams* p, bool* nothing_to_do) {
@@ -121,6 +123,12 @@ void* take_stage_event() {
   return e;
 }
 
+unsigned long long take_wait_limit_ns() {
+  const unsigned long long ns = g_wait_ns;
+  g_wait_ns = kDefaultWaitNs;
+  return ns;
+}
+
 int* device_status_word() {
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
@@ -137,6 +145,8 @@ int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
 void gdn_set_stage_event(void* event) { g_stage_event = event; }
 
+void gdn_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns; }
+
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 size_t gdn_workspace_bytes(const gdn_dims* dims) {
@@ -149,32 +159,10 @@ size_t gdn_workspace_bytes(const gdn_dims* dims) {
 int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
                const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
                void* stream) {
-  g_last_error.clear();
-  if (!dims) return fail(GDN_ERR_ARG, "dims is NULL");
-  int rc = check_token_dims(dims);
-  if (rc) return rc;
-  const bool state_only = dims->flags & GDN_STATE_ONLY;
-  if (dims->n_seqs == 0) return GDN_OK;
-  if (!cu_seqlens || !S_out) return fail(GDN_ERR_ARG, "cu_seqlens and S_out are required");
-  if (!state_only && !O_out) return fail(GDN_ERR_ARG, "O_out is NULL without GDN_STATE_ONLY");
-  if (dims->total_tokens > 0 && (!q || !k || !v || !g || !beta))
-    return fail(GDN_ERR_ARG, "q, k, v, g and beta are required when total_tokens > 0");
-  const void* p16[] = {q, k, v, O_out, S0, S_out};
-  for (const void* p : p16)
-    if (p && !aligned(p, 16)) return fail(GDN_ERR_ALIGN, "q, k, v, O, S0 and S_out must be 16-byte aligned");
-  if (!aligned(g, 4) || !aligned(beta, 4) || !aligned(cu_seqlens, 4))
-    return fail(GDN_ERR_ALIGN, "g, beta and cu_seqlens must be 4-byte aligned");
-  int* status = device_status_word();
-  if (!status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
-
-  SimtParams p{};
-  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = cu_seqlens; p.S0 = S0;
-  p.O = state_only ? nullptr : O_out;
-  p.S_out = S_out; p.T_out = nullptr;
-  p.n_seqs = dims->n_seqs; p.total_tokens = dims->total_tokens;
-  p.h_k = dims->h_k; p.h_v = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
-  p.augmented = 0; p.l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
-  p.write_O = state_only ? 0 : 1; p.scale = dims->scale; p.status = status;
+  SimtParams p;
+  bool nothing = false;
+  const int rc = check_replay_args(dims, q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, &p, &nothing);
+  if (rc || nothing) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dims->dtype == GDN_BF16 && !(dims->flags & GDN_PRECISE) && replay_tc_supported(p)) {
     const size_t bytes = replay_tc_workspace_bytes(p.n_seqs, p.total_tokens, p.h_v);
@@ -270,6 +258,8 @@ int gdn_compose(const gdn_dims* dims, int32_t K, const float* const* T, const fl
   if (S_in && S_in == S_out) return fail(GDN_ERR_ARG, "S_out aliases S_in");
   p.S_in = S_in; p.S_out = S_out; p.K = K; p.h = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
   p.status = device_status_word();
+  if (!p.status) return fail(GDN_ERR_CUDA, "cannot resolve the device status word");
+  p.wait_ns = take_wait_limit_ns();
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = compose_tc_supported(p) ? launch_compose_tc(p, st) : launch_compose_simt(p, st);
   if (e != cudaSuccess) return cuda_fail(e, "gdn_compose launch");

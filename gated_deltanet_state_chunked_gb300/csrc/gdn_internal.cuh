@@ -56,6 +56,7 @@ struct ComposeParams {
   const float* S_in;
   float* S_out;
   int* status;  // sticky device status word (bounded waits that give up report GDN_ERR_TIMEOUT)
+  unsigned long long wait_ns;  // limit of each bounded wait (0: give up unless already complete)
   int K, h, d_k, d_v;
 };
 
@@ -74,5 +75,7 @@ int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const 
 int report_error(int code, const char* message);
 // The event set by gdn_set_stage_event on this thread (nullptr if none); clears it.
 void* take_stage_event();
+// The wait limit set by gdn_set_wait_limit_ns on this thread (else the 2 s default); clears it.
+unsigned long long take_wait_limit_ns();
 
 }  // namespace gdn

@@ -248,16 +248,19 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
   const Tin* __restrict__ v = static_cast<const Tin*>(p.v);
 
   // cu == nullptr: a single sequence covering every token
+  // A malformed range (see chunk_info) is skipped and reported; in two-pass mode `first` is the
+  // global index of this sequence's first chunk in the records.
+  int first = 0;
+  if (p.cu) {
+    const tcp::ChunkInfo ci = tcp::chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, sm.scratch);
+    if (!ci.valid) {
+      if (tid == 0) atomicExch(p.status, GDN_ERR_SHAPE);
+      return;
+    }
+    first = ci.first;
+  }
   const int t_begin = p.cu ? p.cu[seq] : 0;
   const int t_end = p.cu ? p.cu[seq + 1] : p.total_tokens;
-  if (t_begin < 0 || t_end < t_begin || t_end > p.total_tokens) {
-    if (tid == 0) atomicExch(p.status, GDN_ERR_SHAPE);
-    return;
-  }
-
-  // two-pass mode: global index of this sequence's first chunk in the records
-  int first = 0;
-  if (p.rec && p.cu) first = tcp::chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, sm.scratch).first;
 
   // entering state of this slice
   for (int i = tid; i < RS * DK; i += NT) {

@@ -540,12 +540,13 @@ __global__ void __launch_bounds__(NT, 1)
   const int row0 = slice * R;
   const int hk = h / (p.h_v / p.h_k);
 
-  const int t_begin = p.cu[seq], t_end = p.cu[seq + 1];
-  if (t_begin < 0 || t_end < t_begin || t_end > p.total_tokens) {
+  // A malformed range (see chunk_info) has no records: report it before forming any address.
+  const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
+  if (!ci.valid) {
     if (tid == 0) atomicExch(p.status, GDN_ERR_SHAPE);
     return;
   }
-  const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
+  const int t_begin = p.cu[seq], t_end = p.cu[seq + 1];
   const int nch = chunks_of(t_end - t_begin);
 
   if (warp == 0) {
@@ -1056,23 +1057,14 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(96) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch, resolved once per device with that device current
-// (in host code the symbol itself is only a host-side stand-in).
+// Device address of g_static_scratch on the current device.  In host code the symbol itself is
+// only a host-side stand-in, so the address is looked up on every call with the device current
+// (no cached pointer can outlive a device reset).
 int static_scratch_address(void** out) {
-  static std::mutex mu;
-  static void* addr[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return report_error(GDN_ERR_CUDA, "cudaGetDevice failed");
-  if (dev < 0 || dev >= 64) return report_error(GDN_ERR_UNSUPPORTED, "device ordinal out of range");
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-    if (e != cudaSuccess || !ptr) return report_error(GDN_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
-    addr[dev] = ptr;
-  }
-  *out = addr[dev];
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+  if (e != cudaSuccess || !ptr) return report_error(GDN_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+  *out = ptr;
   return GDN_OK;
 }
 
@@ -1093,7 +1085,7 @@ extern "C" int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const voi
     if (need > kStaticScratchBytes)
       return report_error(GDN_ERR_NOMEM,
                           "gdn_replay_noalloc: the problem needs more scratch than the 96 MiB static array "
-                          "((ceil(total_tokens/64) + n_seqs) * h_v * 41984 bytes); use gdn_replay");
+                          "(gdn_workspace_bytes gives the amount); use gdn_replay");
     void* ws = nullptr;
     rc = static_scratch_address(&ws);
     if (rc) return rc;

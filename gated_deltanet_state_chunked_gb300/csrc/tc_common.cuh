@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <climits>
+
 #include "gdn_internal.cuh"
 #include "umma.cuh"
 
@@ -70,12 +72,17 @@ __device__ __forceinline__ uint32_t mnbf16(uint32_t mn, uint32_t k, uint32_t k_r
 
 // Chunk bookkeeping over the packed sequences, block-wide (256 threads).
 // Chunks are numbered globally: sequence s owns ceil(len_s / 64) consecutive
-// numbers.  Returns the number of chunks before sequence `seq` (*first), the
-// total (*total), and, when 0 <= gc < total, the sequence holding global chunk
-// gc (*gc_seq) and its index inside it (*gc_idx).  Malformed ranges count as 0
-// chunks.  scratch: 16 ints of shared memory.
+// numbers.  A range [cu[i], cu[i+1]) counts only when 0 <= cu[i] <= cu[i+1] <=
+// total_tokens and cu[i] is at least every earlier offset (the offsets are
+// non-decreasing up to i); the counted ranges are then disjoint, so they hold
+// at most ceil(total_tokens / 64) + n_seqs chunks, the size of every per-chunk
+// buffer.  Other ranges count as 0 chunks and are not valid.  Returns the number
+// of chunks before sequence `seq` (*first), whether `seq` is valid, the total,
+// and, when 0 <= gc < total, the sequence holding global chunk gc (*gc_seq) and
+// its index inside it (*gc_idx).  scratch: 20 ints of shared memory.
 struct ChunkInfo {
   int first, total, gc_seq, gc_idx;
+  bool valid;
 };
 
 __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
@@ -83,32 +90,53 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (n_seqs == 1) {  // one sequence: no scan over the offsets
     const int a = cu[0], b = cu[1];
-    const int cnt = (a >= 0 && b >= a && b <= total_tokens) ? chunks_of(b - a) : 0;
+    const bool ok = a >= 0 && b >= a && b <= total_tokens;
+    const int cnt = ok ? chunks_of(b - a) : 0;
     ChunkInfo r;
     r.first = seq == 0 ? 0 : cnt;
     r.total = cnt;
+    r.valid = seq == 0 && ok;
     r.gc_seq = (gc >= 0 && gc < cnt) ? 0 : -1;
     r.gc_idx = (gc >= 0 && gc < cnt) ? gc : 0;
     __syncthreads();
     return r;
   }
-  if (tid == 0) { scratch[8] = 0; scratch[9] = -1; scratch[10] = 0; }
+  if (tid == 0) { scratch[16] = 0; scratch[17] = -1; scratch[18] = 0; scratch[19] = 0; }
   __syncthreads();
-  int carry = 0;
+  int carry = 0;                // chunks of the ranges before this block of 256
+  int carry_max = cu[0];        // largest offset before this block's ranges
   for (int base = 0; base < n_seqs; base += 256) {
     const int i = base + tid;
-    int cnt = 0;
-    if (i < n_seqs) {
-      const int a = cu[i], b = cu[i + 1];
-      cnt = (a >= 0 && b >= a && b <= total_tokens) ? chunks_of(b - a) : 0;
-    }
-    int incl = cnt;
+    int a = 0, b = INT_MIN;
+    if (i < n_seqs) { a = cu[i]; b = cu[i + 1]; }
+    // largest end offset of the ranges before i: exclusive prefix maximum of b
+    int incl = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
+      if (lane >= o) incl = max(incl, x);
     }
-    if (lane == 31) scratch[warp] = incl;
+    int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = INT_MIN;
+    if (lane == 31) scratch[8 + warp] = incl;
+    __syncthreads();
+    int wmax = INT_MIN, allmax = INT_MIN;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int m = scratch[8 + w];
+      if (w < warp) wmax = max(wmax, m);
+      allmax = max(allmax, m);
+    }
+    const int before = max(carry_max, max(wmax, excl));
+    const bool ok = i < n_seqs && a >= 0 && a >= before && b >= a && b <= total_tokens;
+    const int cnt = ok ? chunks_of(b - a) : 0;
+    int inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += x;
+    }
+    if (lane == 31) scratch[warp] = inc;
     __syncthreads();
     int wsum = 0, all = 0;
 #pragma unroll
@@ -117,17 +145,19 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
       if (w < warp) wsum += s;
       all += s;
     }
-    const int excl = carry + wsum + incl - cnt;
-    if (i < n_seqs && i == seq) scratch[8] = excl;
-    if (i < n_seqs && cnt > 0 && gc >= excl && gc < excl + cnt) { scratch[9] = i; scratch[10] = gc - excl; }
+    const int ex = carry + wsum + inc - cnt;
+    if (i < n_seqs && i == seq) { scratch[16] = ex; scratch[19] = ok ? 1 : 0; }
+    if (cnt > 0 && gc >= ex && gc < ex + cnt) { scratch[17] = i; scratch[18] = gc - ex; }
     carry += all;
+    carry_max = max(carry_max, allmax);
     __syncthreads();
   }
   ChunkInfo r;
-  r.first = (seq >= 0 && seq < n_seqs) ? scratch[8] : carry;
+  r.first = (seq >= 0 && seq < n_seqs) ? scratch[16] : carry;
+  r.valid = (seq >= 0 && seq < n_seqs) && scratch[19] != 0;
   r.total = carry;
-  r.gc_seq = scratch[9];
-  r.gc_idx = scratch[10];
+  r.gc_seq = scratch[17];
+  r.gc_idx = scratch[18];
   __syncthreads();
   return r;
 }

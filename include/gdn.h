@@ -16,8 +16,10 @@
  * [h_v][d_v]; g and beta: fp32 [total_tokens][h_v].  Sequences (replay tails)
  * are packed back to back; cu_seqlens (int32, DEVICE memory, n_seqs + 1
  * entries, non-decreasing, cu_seqlens[n_seqs] <= total_tokens) gives each
- * one's token range.  v-head h reads q/k head h / (h_v / h_k) (consecutive
- * v-heads share a key head).  States: fp32 [n_seqs][h_v][d_v][d_k].
+ * one's token range.  A range that breaks this (negative, past total_tokens,
+ * or starting before an earlier offset) is skipped, its state left untouched,
+ * and reported as GDN_ERR_SHAPE through gdn_get_status.  v-head h reads q/k
+ * head h / (h_v / h_k) (consecutive v-heads share a key head).  States: fp32 [n_seqs][h_v][d_v][d_k].
  *
  * Ownership and memory.  Every pointer except the host arrays of gdn_compose
  * is a DEVICE pointer owned by the caller; the library never frees or keeps
@@ -116,12 +118,14 @@ int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v
  * loads the library holds until the process exits.
  *   Arguments, layouts, results and error codes are those of gdn_replay.
  *   Limit: the tensor-core path needs (ceil(total_tokens / 64) + n_seqs) * h_v
- *   * 41984 bytes of scratch (a 3277-token tail at 32 v-heads needs 67.9 MiB);
- *   a larger problem is rejected with GDN_ERR_NOMEM before anything is
- *   launched.  fp32 inputs and GDN_PRECISE need no scratch.
- *   The first call on a device resolves the static array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   * 41984 bytes of scratch, plus 4 * n_seqs bytes when n_seqs > 1
+ *   (gdn_workspace_bytes gives the exact figure; a 3277-token tail at 32
+ *   v-heads needs 67.9 MiB); a larger problem is rejected with GDN_ERR_NOMEM
+ *   before anything is launched.  fp32 inputs and GDN_PRECISE need no scratch.
+ *   Every call looks up the static array's device address (cudaGetSymbolAddress,
+ *   with the caller's current device); the first lookup on a device can load
+ *   the library's device code, so make the first call before any stream
+ *   capture.
  *   All calls share the one array: calls that overlap on the GPU (on two
  *   streams, or from two threads) race with each other and must be serialised
  *   by the caller.  Every byte a call reads from the array is written by the
@@ -191,6 +195,18 @@ size_t gdn_workspace_bytes(const gdn_dims* dims);
  * call; the hook is then cleared.  Other calls ignore it.
  */
 void gdn_set_stage_event(void* event);
+
+/*
+ * gdn_set_wait_limit_ns -- test hook for the device-side timeout path (no
+ * counterpart on the pages).  Every wait inside the tensor-core kernels is
+ * bounded (2 s by default): a wait that runs out makes the kernel stop issuing
+ * work, let what it has already issued finish, and report GDN_ERR_TIMEOUT
+ * through gdn_get_status, leaving the context usable.  The next gdn_compose
+ * call made by this thread uses `ns` as that bound (0: a wait gives up unless
+ * its event has already happened, so the call reports a timeout); the hook is
+ * then cleared.  Results of a call that timed out are unspecified.
+ */
+void gdn_set_wait_limit_ns(uint64_t ns);
 
 /* GDN_ABI_VERSION of the loaded library. */
 int gdn_abi_version(void);

@@ -312,3 +312,30 @@ def test_output_scale_is_linear():
     _, O1 = oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, scale=1.0)
     _, O2 = oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, scale=0.125)
     np.testing.assert_allclose(O2, 0.125 * O1, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- the parity metric itself
+
+def test_rel_err_on_hand_computed_vectors():
+    """oracle.rel_err is the one comparison every GPU parity test makes, so it is pinned to
+    values worked out by hand: ||x - ref|| / ||ref|| over the whole tensor, falling back to the
+    absolute norm when ref is zero."""
+    assert oracle.rel_err([3.0, 4.0], [0.0, 0.0]) == 5.0          # zero reference: absolute norm
+    assert oracle.rel_err([1.0, 1.0], [1.0, 0.0]) == 1.0          # |(0,1)| / |(1,0)|
+    assert oracle.rel_err([1.0, 0.0], [1.0, 1.0]) == pytest.approx(2 ** -0.5, rel=1e-15)  # not symmetric
+    # a 2x2 tensor: sqrt(1 + 4) / sqrt(9 + 16) over all elements, not row by row
+    assert oracle.rel_err([[1.0, 2.0], [3.0, 4.0]], [[0.0, 0.0], [3.0, 4.0]]) == pytest.approx(5 ** 0.5 / 5, rel=1e-15)
+    x = np.arange(1.0, 7.0).reshape(2, 3)
+    assert oracle.rel_err(x, x) == 0.0
+    assert oracle.rel_err(3.0 * x, 3.0 * x) == 0.0
+    # one changed element among a thousand is seen, with the value the definition gives
+    ref = np.ones(1000)
+    y = ref.copy()
+    y[517] += 1e-3
+    assert oracle.rel_err(y, ref) == pytest.approx(1e-3 / 1000 ** 0.5, rel=1e-9)
+    assert oracle.rel_err(y, ref) > 0.0
+    # scale invariance: scaling x and ref together leaves it unchanged
+    assert oracle.rel_err(7.0 * y, 7.0 * ref) == pytest.approx(oracle.rel_err(y, ref), rel=1e-12)
+    # float32 inputs are compared in fp64 (the difference is not rounded away)
+    a32 = np.float32(1.0) + np.float32(2 ** -20)
+    assert oracle.rel_err(np.array([a32], np.float32), np.array([1.0], np.float32)) == 2 ** -20

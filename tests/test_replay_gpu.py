@@ -107,6 +107,22 @@ def test_malformed_cu_seqlens_sets_status_and_skips_sequence():
     assert rel_err(host(S[0]), S_ref[0]) <= TOL_F32
 
 
+def test_overlapping_forward_ranges_are_skipped():
+    """[0, T, 0, T]: the ranges after the step back are skipped and reported (fp32 path)."""
+    T = 100
+    x = synthetic.make_replay_inputs([T], 1, 2, 32, 32, dtype="f32", seed=12)
+    d = to_device(x)
+    cu = torch.tensor([0, T, 0, T], dtype=torch.int32, device="cuda")
+    S = torch.full((3, 2, 32, 32), 5.0, device="cuda")
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=True)
+    with pytest.raises(_lib.GdnError) as ei:
+        api.gdn_get_status()
+    assert ei.value.code == _lib.GDN_ERR_SHAPE
+    assert torch.all(S[1] == 5.0) and torch.all(S[2] == 5.0)
+    S_ref, _ = oracle.replay(x.q, x.k, x.v, x.g, x.beta, [0, T], want_O=False)
+    assert rel_err(host(S[0]), S_ref[0]) <= TOL_F32
+
+
 def test_precise_path_on_bf16_inputs():
     x = synthetic.make_replay_inputs(RAGGED, 2, 4, 128, 128, dtype="bf16", seed=12, with_S0=True)
     O, S = _run(x, precise=True)
@@ -180,3 +196,25 @@ def test_composed_chunks_equal_sequential_replay():
     S_ref, _ = oracle_replay(x, want_O=False)
     assert rel_err(host(SK), S_ref[0]) <= TOL_F32
     assert rel_err(host(S[0]), S_ref[0]) <= TOL_F32
+
+
+@pytest.mark.parametrize("K", [1, 5])
+def test_compose_wait_that_runs_out_reports_timeout_then_recovers(K):
+    """The bounded-wait path without a fault: with a wait limit of zero the first wait on the
+    MMAs gives up, the kernel lets its issued MMAs finish and reports GDN_ERR_TIMEOUT; the
+    context stays usable and the next call (default limit) is correct."""
+    rng = np.random.Generator(np.random.PCG64(60 + K))
+    h, d = 4, 128
+    T = (rng.standard_normal((K, h, d, d)) / np.sqrt(d)).astype(np.float32)
+    Sl = rng.standard_normal((K, h, d, d)).astype(np.float32)
+    Td = [torch.from_numpy(T[j]).cuda() for j in range(K)]
+    Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
+    api.gdn_set_wait_limit_ns(0)
+    api.gdn_compose(Td, Sd, None)
+    with pytest.raises(_lib.GdnError) as ei:
+        api.gdn_get_status()
+    assert ei.value.code == _lib.GDN_ERR_TIMEOUT
+    out = api.gdn_compose(Td, Sd, None)  # the hook was cleared: default bound
+    torch.cuda.synchronize()
+    api.gdn_get_status()
+    assert rel_err(host(out), oracle.compose(T, Sl, None)) <= TOL_F32

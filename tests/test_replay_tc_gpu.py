@@ -153,6 +153,23 @@ def test_malformed_cu_seqlens_reports_shape_error():
     assert torch.all(S[1] == 9.0)
 
 
+def test_overlapping_forward_ranges_report_shape_error():
+    """Offsets that each run forward but go back ([0, T, 0, T]) would hold more chunks than the
+    per-chunk buffers: the ranges after the step back are skipped and reported, nothing else."""
+    T = 200
+    x = synthetic.make_replay_inputs([T], 2, 4, 128, 128, dtype="bf16", seed=310)
+    d = to_device(x)
+    cu = torch.tensor([0, T, 0, T], dtype=torch.int32, device="cuda")
+    S = torch.full((3, 4, 128, 128), 7.0, device="cuda")
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=True)
+    with pytest.raises(_lib.GdnError) as ei:
+        api.gdn_get_status()
+    assert ei.value.code == _lib.GDN_ERR_SHAPE
+    assert torch.all(S[1] == 7.0) and torch.all(S[2] == 7.0)
+    S_ref, _ = oracle.replay(x.q, x.k, x.v, x.g, x.beta, [0, T], want_O=False)
+    assert rel_err(host(S[0]), S_ref[0]) <= TOL_BF16
+
+
 def test_repeated_calls_are_deterministic():
     x = synthetic.make_replay_inputs([777], 2, 4, 128, 128, dtype="bf16", seed=309)
     O1, S1 = _run(x)

@@ -6,7 +6,8 @@ starts and forbids allocations afterwards).  gdn_replay_noalloc serves them by
 taking its scratch from a fixed static device array instead of a pool.  This
 test calls it through the C ABI twice in a row, on different inputs (so a stale
 array from the first call would show in the second), and checks each result
-against gdn_replay's at the tolerance of the other bf16 parity tests.  It also
+against gdn_replay's and against the fp64 oracle's at the tolerance of the
+other bf16 parity tests.  It also
 checks that a problem larger than the static array is refused up front.  The
 file is named so that pytest collects it last.
 """
@@ -38,12 +39,16 @@ def _both(x):
 
 
 def test_matches_gdn_replay_on_two_calls_in_a_row():
+    """Each call's result agrees with gdn_replay's and with the fp64 oracle's."""
     first = synthetic.make_replay_inputs([700, 333, 64], 2, 4, 128, 128, dtype="bf16", seed=501, with_S0=True)
     second = synthetic.make_replay_inputs([1300, 5], 2, 4, 128, 128, dtype="bf16", seed=502, unit_qk=False)
     for x in (first, second):
         (O, S), (O_ref, S_ref) = _both(x)
         assert rel_err(host(S), host(S_ref)) <= TOL_BF16
         assert rel_err(host(O), host(O_ref)) <= TOL_BF16
+        S_or, O_or = oracle_replay(x)
+        assert rel_err(host(S), S_or) <= TOL_BF16
+        assert rel_err(host(O), O_or) <= TOL_BF16
 
 
 @pytest.mark.parametrize("d_k,d_v", [(128, 128), (64, 32)])
@@ -67,6 +72,9 @@ def test_single_layer_3277_token_tail_fits():
     (O, S), (O_ref, S_ref) = _both(x)
     assert rel_err(host(S), host(S_ref)) <= TOL_BF16
     assert rel_err(host(O), host(O_ref)) <= TOL_BF16
+    S_or, O_or = oracle_replay(x)
+    assert rel_err(host(S), S_or) <= TOL_BF16
+    assert rel_err(host(O), O_or) <= TOL_BF16
 
 
 def test_rejects_a_problem_beyond_the_static_scratch():
