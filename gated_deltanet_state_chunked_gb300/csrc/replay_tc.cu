@@ -429,18 +429,22 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 // ---------------------------------------------------------------------------------------------
 template <int R>
 struct ScanLay {
-  // With 32-row slices K has three buffers and Q two, so that a chunk's K and Q are copied a
-  // whole chunk ahead (the prep warps otherwise wait for them); with 64-row slices (the
-  // throughput case, where that measured slower) K has two and Q one, copied once the chain
-  // has finished the chunk two before.
-  static constexpr bool EARLY_KQ = R == 32;
+  // 32-row slices (the latency case, few problems): every tile a chunk needs is requested a
+  // whole chunk ahead (K has three buffers, Q two), M diag(beta) and P are A operands in TMEM
+  // (a 64-column region shared by both: Mb in lanes 0-63, P in lanes 64-127; each product's
+  // other 64 rows are results nobody reads), and K^T [U^hi | U^lo] is one product of N = 2R
+  // that reads K^T once.  64-row slices (the throughput case) have no TMEM columns to spare:
+  // Mb and P are read from shared memory, K and Q are copied once the chain has finished the
+  // chunk two before (two K buffers, one Q), and K^T U^ runs over K = [tokens; tokens].
+  static constexpr bool NARROW = R == 32;
+  static constexpr bool EARLY_KQ = NARROW;
   static constexpr int NKB = EARLY_KQ ? 3 : 2, NQB = EARLY_KQ ? 2 : 1;
   static constexpr uint32_t KB = 0;                 // NKB buffers of bf16 K: 2 d_k atoms x (64 rows x 128 B)
   static constexpr uint32_t QB = KB + NKB * 16384;  // NQB buffers of bf16 Q: 2 d_k atoms x (64 rows x 128 B)
   static constexpr uint32_t VT = QB + NQB * 16384;  // bf16 V atom: 64 tokens x 128 B
   static constexpr uint32_t R1 = VT + 8192;         // record part 1: Mb hi|lo (16 KB), Mw (8 KB)
   static constexpr uint32_t R2 = R1 + kRecPart1;    // 2 buffers of record part 2: P (16 KB), factors (1 KB)
-  static constexpr uint32_t UH = R2 + 2 * 18432;    // bf16 [U^hi;U^lo] MN-major (128 token rows x 128 B)
+  static constexpr uint32_t UH = R2 + 2 * 18432;    // bf16 U^ hi and lo, MN-major (see the U epilogue)
   static constexpr uint32_t UT = UH + 16384;        // fp32 U^T (R rows x 2 atoms)
   static constexpr uint32_t S32 = UT + R * 256;     // fp32 state slice (R rows x 4 atoms), tf32-rounded
   static constexpr uint32_t BARS = S32 + R * 512;
@@ -448,20 +452,20 @@ struct ScanLay {
   static constexpr uint32_t ALLOC = TOTAL + 1024;
   // TMEM columns.  All accumulators use the M=128 layout (lane = row).  cWQ holds the fp32
   // [W;Q] operand of [W;Q] S0^T (lane = token row, column = d_k), read by the MMA straight from
-  // TMEM.  [W;Q] S0^T and U~ put the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127
-  // (Q S0^T; P U is aimed there too).  U~ and [W;Q] S0^T have one copy per chunk parity: a
-  // chunk's outputs are read back while the next chunk's [W;Q] S0^T runs.  P U has one copy:
-  // the next P U is issued only after the outputs have read it.
-  // A thread issues small MMAs one after another at a fixed cost each, whatever their size,
-  // while threads in different warps issue side by side; so each product is split by K over
-  // ND1 / ND2 / NPU issuing warps, each into an accumulator of its own, and the epilogues add
-  // the partial sums.  With 64-row slices the columns hold one accumulator per product.
-  static constexpr int ND1 = R == 32 ? 2 : 1, ND2 = R == 32 ? 2 : 1, NPU = R == 32 ? 2 : 1;
-  static_assert(ND1 <= 2 && ND2 <= 2 && NPU <= 2, "the epilogues add at most two partial sums");
-  // accumulator a of [W;Q] S0^T for chunk parity b: cD1 + (2 a + b) R; of K^T U^ and P U: + a R
-  static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = cD1 + 2 * R * ND1, cPU = cD2 + R * ND2;
+  // TMEM (as tf32: the low mantissa bits of W are dropped, Q is exact).  [W;Q] S0^T and U~ put
+  // the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127 (Q S0^T; P U is aimed there too).
+  // U~ and [W;Q] S0^T have one copy per chunk parity: a chunk's outputs are read back while the
+  // next chunk's [W;Q] S0^T runs.  P U has one copy: the next P U is issued only after the
+  // outputs have read it.  Each product is issued by one warp (the tensor pipe takes these
+  // small MMAs one after another whichever warps issue them).
+  static constexpr int ND1 = 1, NPU = 1;
+  // K^T U^: 32-row slices one accumulator of 2R columns ([hi | lo]); 64-row slices R columns
+  static constexpr uint32_t D2COLS = NARROW ? 2 * R : R;
+  // accumulator a of [W;Q] S0^T for chunk parity b: cD1 + (2 a + b) R; of P U: cPU + a R
+  static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = cD1 + 2 * R * ND1, cPU = cD2 + D2COLS;
+  static constexpr uint32_t cMP = cPU + R * NPU;  // (32-row slices) Mb in lanes 0-63, P in lanes 64-127
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(cPU + R * NPU <= TMEM_COLS, "TMEM columns");
+  static_assert(cMP + (NARROW ? 64 : 0) <= TMEM_COLS, "TMEM columns");
   static_assert(ALLOC <= 232448, "shared memory");
   static_assert(QB % 1024 == 0 && R2 % 1024 == 0 && UH % 1024 == 0 && UT % 1024 == 0 &&
                     S32 % 1024 == 0 && R1 >= 8192,
@@ -492,8 +496,8 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
 // f(j, j == J0) for j = J0 .. J1-1, unrolled at compile time (an MMA issue loop whose operand
-// offsets fold to constants: each instruction a thread issues costs it many cycles, so the
-// issue loop carries no arithmetic of its own).
+// offsets fold to constants).  Issue sites run on a whole converged warp with warp-uniform
+// operands; f issues through elect_one().
 template <int J0, int J1, typename F>
 __device__ __forceinline__ void issue_range(F&& f) {
 #pragma unroll
@@ -505,9 +509,8 @@ __device__ __forceinline__ void issue_range(F&& f) {
 // Warps 0-1 form U from the token rows 0-63 of D1 while warps 2-3 write the previous chunk's
 // outputs from rows 64-127 (Q S0^T) and P U, so the output epilogue is off the chunk-to-chunk
 // chain.  Warps 4-7 ("prep") run one chunk ahead: the W = Mw K and U~ MMAs, the [W;Q]
-// operand in TMEM (W rounded to tf32 in place, the Q rows stored beside it) and all loads.
-// The groups hand over through mbarriers that complete once per chunk; MMAs are issued by
-// threads in different warps so that independent streams do not queue behind one issuer.
+// operand in TMEM (the Q rows stored beside W), with 32-row slices Mb and P in TMEM, and all
+// loads.  The groups hand over through mbarriers that complete once per chunk.
 template <int R>
 __global__ void __launch_bounds__(NT, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -525,8 +528,21 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* bar_d1 = bars + 7;   // MMA [W;Q] S0^T
   uint64_t* bar_d2 = bars + 8;   // MMA K^T U^
   uint64_t* bar_pu = bars + 9;   // MMA P U
-  uint64_t* ev_w = bars + 10;    // prep -> chain: [W;Q] operand of the chunk ready in TMEM
-  uint64_t* ev_s = bars + 11;    // [2] chain -> prep: chunk finished (one barrier per chunk parity)
+  constexpr int NBARS = 10;
+  // Hand-offs between the two warp groups are named barriers (an mbarrier hand-off between warps
+  // of one SM costs about 200 cycles, a named barrier about 36).  Each is arrived at by one group
+  // and synchronised on by the other, once per chunk, and every use strictly alternates with the
+  // other side's, by construction (so counts never mix and neither side can wait forever on an
+  // arrival that the other made for a different chunk):
+  //   NB_W  prep -> chain: [W;Q], U~ (and Mb) of chunk c are in TMEM.  The prep arrives for chunk
+  //         c only after NB_S of chunk c-1, which the chain arrives at after it synchronised
+  //         on NB_W of chunk c-1.
+  //   NB_S  chain -> prep: chunk c is finished (its P U has completed, its factors were read).
+  //         The chain arrives for chunk c+1 only after NB_W of chunk c+1.
+  //   NB_P  prep (warps 6-7) -> the P U issuer (warp 1), 32-row slices with outputs: P of chunk
+  //         c is in TMEM.  Arrived at after NB_S of chunk c-1; synchronised on before P U of c,
+  //         which precedes the chain's NB_S of chunk c.  (64 + 32 threads.)
+  constexpr int NB_W = 3, NB_S = 4, NB_P = 5;
   // buffers of chunk c's K and Q tiles
   auto kbuf = [&](int c) { return (uint32_t)(c % L::NKB); };
   auto qbuf = [&](int c) { return (uint32_t)(L::NQB == 2 ? c & 1 : 0); };
@@ -573,8 +589,8 @@ __global__ void __launch_bounds__(NT, 1)
     bulk_load(sm + L::R1, rec_of(c), kRecPart1, bar_r1);
   };
   if (tid == 0) {
-    for (int i = 0; i < 13; ++i) {  // the MMA barriers count one commit per issuing thread
-      const int n = &bars[i] == bar_d1 ? L::ND1 : &bars[i] == bar_d2 ? L::ND2 : &bars[i] == bar_pu ? L::NPU : 1;
+    for (int i = 0; i < NBARS; ++i) {  // the MMA barriers count one commit per issuing warp
+      const int n = &bars[i] == bar_d1 ? L::ND1 : &bars[i] == bar_pu ? L::NPU : 1;
       mbar_init(&bars[i], n);
     }
     mbar_fence_init();
@@ -620,10 +636,14 @@ __global__ void __launch_bounds__(NT, 1)
   const uint64_t dUT = sdesc_sw128(smem_u32(sm + L::UT), 16, 1024);
   const uint64_t dS32 = sdesc_sw128(smem_u32(sm + L::S32), 16, 1024);
   // Bounded wait.  After the first timeout every later wait returns at once, so both
-  // warp groups run their (uniform) loops to the end and the CTA exits with an error.
+  // warp groups run their (uniform) loops to the end and the CTA exits with an error.  The chain
+  // warps poll (their waits are on MMAs that finish within a few hundred cycles, on the critical
+  // path); the prep warps, which run ahead and wait long, suspend so that they leave the issue
+  // slots of their schedulers to the chain warps.
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (flags[0]) return;
-    if (!mbar_wait(bar, parity, kWaitNs)) flags[0] = 1;
+    const bool ok = chain ? mbar_wait_spin(bar, parity, kWaitNs) : mbar_wait(bar, parity, kWaitNs);
+    if (!ok) flags[0] = 1;
   };
 
   if (chain) {
@@ -634,6 +654,7 @@ __global__ void __launch_bounds__(NT, 1)
     auto outputs = [&](int cc) {
       const uint32_t pb = (uint32_t)(cc & 1) * R;
       const int t0c = t_begin + cc * C, n = min(C, t_end - t0c);
+      wait(bar_pu, (uint32_t)(cc & 1));  // P U of chunk cc
       tc_fence_after();
 #pragma unroll
       for (int hh = 0; hh < R / 32; ++hh) {  // 32 state rows at a time
@@ -672,13 +693,14 @@ __global__ void __launch_bounds__(NT, 1)
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1;
       const float* gate = reinterpret_cast<const float*>(sm + L::R2 + par * 18432 + (kRecGate - kRecPart1));
-      wait(ev_w, par);
-      if (lane == 0 && warp < L::ND1) {  // D1 = [W;Q] S0^T (tf32, [W;Q] from TMEM: 8 columns per K step)
+      named_sync(NB_W, 256);
+      if (warp < L::ND1) {  // D1 = [W;Q] S0^T (tf32, [W;Q] from TMEM: 8 columns per K step)
         tc_fence_after();
         constexpr uint32_t id1 = idesc_tf32(128, R);
         const uint32_t dst = tmem + L::cD1 + (2 * warp + par) * R;
         auto d1 = [&](int j, bool first) {
-          mma_tf32_ts(dst, tmem + L::cWQ + 8 * j, dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, !first);
+          if (elect_one())
+            mma_tf32_ts(dst, tmem + L::cWQ + 8 * j, dadd(dS32, (j >> 2) * (R * 128) + (j & 3) * 32), id1, !first);
         };
         if constexpr (L::ND1 == 1) {
           issue_range<0, 16>(d1);
@@ -686,10 +708,11 @@ __global__ void __launch_bounds__(NT, 1)
           if (warp == 0) issue_range<0, 8>(d1);
           else issue_range<8, 16>(d1);
         }
-        mma_commit(bar_d1);
+        if (elect_one()) mma_commit(bar_d1);
+        __syncwarp();
       }
-      wait(bar_r2 + par, (c >> 1) & 1);  // factors and P of this chunk
-      if (quad < 2) {  // U = U~ - W S0^T (token t); U^ hi|lo MN-major, U^T tf32
+      // (the factors of this chunk have landed: the prep waited for them before NB_W)
+      if (quad < 2) {  // U = U~ - W S0^T (token t); U^ hi and lo (MN-major), U^T tf32
         wait(bar_d1, par);
         tc_fence_after();
         const float sc = gate[64 + t];
@@ -725,8 +748,13 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             const int r = 32 * hh + i;
-            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, t, 128)) = *reinterpret_cast<const uint4*>(hp + i / 2);
-            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lp + i / 2);
+            if constexpr (L::NARROW) {  // N = 2R: hi in MN columns [0, R), lo in [R, 2R); K = 64 tokens
+              *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, t, 64)) = *reinterpret_cast<const uint4*>(hp + i / 2);
+              *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(R + r, t, 64)) = *reinterpret_cast<const uint4*>(lp + i / 2);
+            } else {  // K = 128: hi in token rows 0-63, lo in 64-127
+              *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, t, 128)) = *reinterpret_cast<const uint4*>(hp + i / 2);
+              *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lp + i / 2);
+            }
           }
         }
       } else if (p.write_O && c > 0) {
@@ -735,44 +763,52 @@ __global__ void __launch_bounds__(NT, 1)
       fence_async_smem();
       tc_fence_before();
       group_sync(1);
-      // K^T U^ (state) from warps 0 (and 2), P U (outputs, P in rows 64-127) from warps 1 (and 3)
-      if (lane == 0 && (warp & 1) == 0 && (warp >> 1) < L::ND2) {
+      // K^T U^ (state) from warp 0, P U (outputs, P in rows 64-127) from warps 1 (and 3)
+      if (warp == 0) {
         tc_fence_after();
-        constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
         const uint64_t dk = dadd(dKmn, kbuf(c) * 16384u);
-        const uint32_t dst = tmem + L::cD2 + (warp >> 1) * R;
-        auto d2 = [&](int j, bool first) {
-          mma_bf16(dst, dadd(dk, (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, !first);
-        };
-        if constexpr (L::ND2 == 1) {
+        if constexpr (L::NARROW) {  // [K^T U^hi | K^T U^lo]: N = 2R, four K steps of 16 tokens
+          constexpr uint32_t id2 = idesc_bf16(128, 2 * R, true, true);
+          auto d2 = [&](int j, bool first) {
+            if (elect_one()) mma_bf16(tmem + L::cD2, dadd(dk, j * 2048), dadd(dUHmn, j * 2048), id2, !first);
+          };
+          issue_range<0, 4>(d2);
+        } else {  // [K^T | K^T] [U^hi; U^lo]: K = 128
+          constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
+          auto d2 = [&](int j, bool first) {
+            if (elect_one())
+              mma_bf16(tmem + L::cD2, dadd(dk, (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, !first);
+          };
           issue_range<0, 8>(d2);
-        } else {
-          if (warp == 0) issue_range<0, 4>(d2);
-          else issue_range<4, 8>(d2);
         }
-        mma_commit(bar_d2);
-      } else if (lane == 0 && (warp & 1) == 1 && (warp >> 1) < L::NPU && p.write_O) {
-        tc_fence_after();
-        constexpr uint32_t idp = idesc_tf32(128, R);
-        const uint64_t dp = dadd(dR2p, par * 18432);
+        if (elect_one()) mma_commit(bar_d2);
+        __syncwarp();
+      } else if ((warp & 1) == 1 && (warp >> 1) < L::NPU && p.write_O) {
         const uint32_t dst = tmem + L::cPU + (warp >> 1) * R;
-        auto pu = [&](int j, bool first) {
-          mma_tf32(dst, dadd(dp, (j >> 2) * 8192 + (j & 3) * 32), dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp,
-                   !first);
-        };
-        if constexpr (L::NPU == 1) {
+        constexpr uint32_t idp = idesc_tf32(128, R);
+        if constexpr (L::NARROW) {  // A = P from TMEM (lanes 64-127 of cMP)
+          named_sync(NB_P, 96);
+          tc_fence_after();
+          auto pu = [&](int j, bool first) {
+            if (elect_one())
+              mma_tf32_ts(dst, tmem + L::cMP + 8 * j, dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32), idp, !first);
+          };
           issue_range<0, 8>(pu);
         } else {
-          if (warp == 1) issue_range<0, 4>(pu);
-          else issue_range<4, 8>(pu);
+          tc_fence_after();
+          const uint64_t dp = dadd(dR2p, par * 18432);
+          auto pu = [&](int j, bool first) {
+            if (elect_one())
+              mma_tf32(dst, dadd(dp, (j >> 2) * 8192 + (j & 3) * 32), dadd(dUT, (j >> 2) * (R * 128) + (j & 3) * 32),
+                       idp, !first);
+          };
+          issue_range<0, 8>(pu);
         }
-        mma_commit(bar_pu);
+        if (elect_one()) mma_commit(bar_pu);
+        __syncwarp();
       }
+      if (p.write_O) gq_prev = gate[128 + t];  // output gate of this chunk (written out in the next)
       wait(bar_d2, par);
-      if (p.write_O) {  // P U has read P: its buffer may be refilled once the chunk is done
-        wait(bar_pu, par);
-        gq_prev = gate[128 + t];
-      }
       tc_fence_after();
       {  // S <- gamma_C S + K^T U^ (M=128 layout: lane = d_k)
         const float gC = gate[63];
@@ -780,13 +816,13 @@ __global__ void __launch_bounds__(NT, 1)
         for (int hh = 0; hh < R / 32; ++hh) {
           float d2[32], x[32];
           tmem_ld32(tmem + lane_base + L::cD2 + 32 * hh, d2);
-          if constexpr (L::ND2 == 2) tmem_ld32(tmem + lane_base + L::cD2 + R + 32 * hh, x);
+          if constexpr (L::NARROW) tmem_ld32(tmem + lane_base + L::cD2 + R + 32 * hh, x);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {  // packed pairs (same rounding as the scalar forms)
             const int r = 32 * hh + i;
             float2 d = make_float2(d2[i], d2[i + 1]);
-            if constexpr (L::ND2 == 2) d = __fadd2_rn(d, make_float2(x[i], x[i + 1]));
+            if constexpr (L::NARROW) d = __fadd2_rn(d, make_float2(x[i], x[i + 1]));
             const float2 sn = __ffma2_rn(make_float2(gC, gC), make_float2(sreg[r], sreg[r + 1]), d);
             sreg[r] = sn.x;
             sreg[r + 1] = sn.y;
@@ -797,63 +833,79 @@ __global__ void __launch_bounds__(NT, 1)
       }
       fence_async_smem();
       tc_fence_before();
-      group_sync(1);
-      if (tid == 0) mbar_arrive(&ev_s[par]);
+      named_arrive(NB_S, 256);
     }
     if (p.write_O && nch > 0 && quad >= 2) outputs(nch - 1);
   } else {
     // ============================================================ prep warps
-    const bool issW = tid == 128, issU = tid == 192;
+    const int t = 32 * (quad & 1) + lane;  // token of this thread's TMEM lane (rows of its quarter)
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1;
       // (three K, two Q buffers) K and Q of chunk c+1, a chunk ahead: K goes to the buffer of
       // chunk c-2, Q to that of chunk c-1; their readers (W, K^T U^ of c-2; the Q rows of c-1)
       // finished before the chain ended chunk c-2, which the previous iteration waited for.
       // bar_kq[(c+1)&1] last completed for chunk c-1, also waited for: no phase overrun.
-      if (L::EARLY_KQ && issU && c + 1 < nch) load_kq(c + 1);
+      if (L::EARLY_KQ && warp == 6 && elect_one() && c + 1 < nch) load_kq(c + 1);
+      __syncwarp();
       wait(bar_kq + par, (c >> 1) & 1);
       wait(bar_r1, par);
       if (c > 0) wait(bar_d1, (c - 1) & 1);  // the previous [W;Q] S0^T has read the [W;Q] columns
-      if (issW) {  // W = Mw K into the [W;Q] columns (M=128: rows 64-127 are replaced by Q below)
+      if constexpr (L::NARROW) {
+        // Mb (hi | lo, bf16 pairs) into lanes 0-63 of cMP: U~ of the previous chunk has read them
+        // (its completion was waited for below); P U may still read these lanes as rows nobody uses.
+        if (quad < 2) {
+#pragma unroll 1
+          for (int a = 0; a < 2; ++a) {  // a = 0: hi (K 0-63), a = 1: lo (K 64-127)
+            float v[32];  // column j holds K elements (2j, 2j + 1) as a bf16 pair
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::R1 + kRecMB + kbf16(t, 64 * a + 8 * ch, 64));
+              v[4 * ch] = __uint_as_float(raw.x);
+              v[4 * ch + 1] = __uint_as_float(raw.y);
+              v[4 * ch + 2] = __uint_as_float(raw.z);
+              v[4 * ch + 3] = __uint_as_float(raw.w);
+            }
+            tmem_st32(tmem + lane_base + L::cMP + 32 * a, v);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        group_sync(2);
+      }
+      if (warp == 4) {  // W = Mw K into the [W;Q] columns (M=128: rows 64-127 are replaced by Q below)
         tc_fence_after();
         constexpr uint32_t idW = idesc_bf16(128, 128, false, true);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_bf16(tmem + L::cWQ, dadd(dR1, kRecMW + j * 32), dadd(dKmn, kbuf(c) * 16384 + j * 2048), idW, j > 0);
-        mma_commit(bar_w);
-      } else if (issU) {  // U~ = [Mb_hi|Mb_lo][V;V] (M=128: rows 64-127 are not used)
+          if (elect_one())
+            mma_bf16(tmem + L::cWQ, dadd(dR1, kRecMW + j * 32), dadd(dKmn, kbuf(c) * 16384 + j * 2048), idW, j > 0);
+        if (elect_one()) mma_commit(bar_w);
+        __syncwarp();
+      } else if (warp == 6) {  // U~ = [Mb_hi|Mb_lo][V;V] (M=128: rows 64-127 are not used)
         tc_fence_after();
         constexpr uint32_t idU = idesc_bf16(128, R, false, true);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          mma_bf16(tmem + L::cU + par * R, dadd(dR1, kRecMB + (j >> 2) * 8192 + (j & 3) * 32),
-                   dadd(dVT, (j & 3) * 2048), idU, j > 0);
-        mma_commit(bar_u);
+        for (int j = 0; j < 8; ++j) {
+          if (elect_one()) {
+            if constexpr (L::NARROW)
+              mma_bf16_ts(tmem + L::cU + par * R, tmem + L::cMP + 8 * j, dadd(dVT, (j & 3) * 2048), idU, j > 0);
+            else
+              mma_bf16(tmem + L::cU + par * R, dadd(dR1, kRecMB + (j >> 2) * 8192 + (j & 3) * 32),
+                       dadd(dVT, (j & 3) * 2048), idU, j > 0);
+          }
+        }
+        if (elect_one()) mma_commit(bar_u);
+        __syncwarp();
       }
       wait(bar_w, par);
       wait(bar_u, par);
       tc_fence_after();
       group_sync(2);
-      if (issU && c + 1 < nch) load_r1(c + 1);  // V and record part 1 are free
-      if (quad < 2) {  // W rows (token = TMEM lane) rounded to nearest tf32 in place: the MMA
-                       // reading them from TMEM would otherwise drop the low mantissa bits
-#pragma unroll
-        for (int cc = 0; cc < 4; cc += 2) {
-          float v[32], w[32];
-          tmem_ld32(tmem + lane_base + L::cWQ + cc * 32, v);
-          tmem_ld32(tmem + lane_base + L::cWQ + cc * 32 + 32, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = tf32r(v[i]);
-            w[i] = tf32r(w[i]);
-          }
-          tmem_st32(tmem + lane_base + L::cWQ + cc * 32, v);
-          tmem_st32(tmem + lane_base + L::cWQ + cc * 32 + 32, w);
-        }
-      } else if (p.write_O) {  // Q rows (token 32*(quad-2) + lane): bf16, exact in fp32
+      if (warp == 6 && elect_one() && c + 1 < nch) load_r1(c + 1);  // V and record part 1 are free
+      __syncwarp();
+      if (quad >= 2 && p.write_O) {  // Q rows (token 32*(quad-2) + lane): bf16, exact in fp32
         const int tq = 32 * (quad - 2) + lane;
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {  // d_k columns [32 cc, 32 cc + 32)
           float v[32];
 #pragma unroll
@@ -868,22 +920,49 @@ __global__ void __launch_bounds__(NT, 1)
           }
           tmem_st32(tmem + lane_base + L::cWQ + cc * 32, v);
         }
+        tmem_st_wait();
       }
-      tmem_st_wait();
       tc_fence_before();
-      group_sync(2);
-      // The tile is published before waiting for the chain to finish chunk c-1, so the chain
-      // starts chunk c without a round trip.  ev_s has one barrier per chunk parity, and the
-      // chain cannot finish chunk c+1 before this arrival, so the wait below never finds its
-      // barrier two phases ahead.
-      if (issW) mbar_arrive(ev_w);
-      if (c > 0) wait(&ev_s[(c - 1) & 1], ((c - 1) >> 1) & 1);  // the chain has finished chunk c-1
-      if (issU && c + 1 < nch) {
+      // Publish chunk c once the chain has finished chunk c-1 (it then finds this chunk's
+      // operands ready and continues with a named-barrier round trip), and once record part 2
+      // (factors and P) of chunk c has landed: the chain reads the factors without waiting.
+      wait(bar_r2 + par, (c >> 1) & 1);
+      if (c > 0) named_sync(NB_S, 256);
+      named_arrive(NB_W, 256);
+
+      if constexpr (L::NARROW) {
+        // P of chunk c into lanes 64-127 of cMP (P U of chunk c-1 has completed: the chain
+        // finished that chunk), then tell the P U issuers.
+        if (quad >= 2 && p.write_O) {
+          if (c > 0) wait(bar_pu, (c - 1) & 1);  // P U of chunk c-1 has read lanes 64-127 of cMP
+          tc_fence_after();
+          const unsigned char* P = sm + L::R2 + par * 18432 + (kRecP - kRecPart1);
+#pragma unroll 1
+          for (int a = 0; a < 2; ++a) {  // tokens s in [32 a, 32 a + 32)
+            float v[32];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const float4 x = *reinterpret_cast<const float4*>(P + kf32(t, 32 * a + 4 * ch, 64));
+              v[4 * ch] = x.x;
+              v[4 * ch + 1] = x.y;
+              v[4 * ch + 2] = x.z;
+              v[4 * ch + 3] = x.w;
+            }
+            tmem_st32(tmem + lane_base + L::cMP + 32 * a, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          named_arrive(NB_P, 96);
+        }
+      }
+      if (warp == 6 && elect_one() && c + 1 < nch) {
         // (two K, one Q buffer) K of chunk c-1 and the Q staging buffer have no readers left
         if (!L::EARLY_KQ) load_kq(c + 1);
         if (c >= 1) load_r2(c + 1);  // P and factors of chunk c-1 are no longer read
       }
+      __syncwarp();
     }
+    if (nch > 0) named_sync(NB_S, 256);  // the chain's arrival for its last chunk
   }
 
   __syncthreads();

@@ -164,6 +164,15 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
 
 // Named barrier over one 128-thread warpgroup (ids 1, 2, ...; 0 is __syncthreads).
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+// Producer / consumer hand-off on named barrier `id` with `count` participating threads in all
+// (a multiple of 32): producers arrive without waiting, consumers wait until every participant
+// has reached it.  Memory operations before the arrival are visible to the consumers after it.
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 constexpr int MST = 68;  // row stride (floats) of the 64x64 fp32 work matrices (16-byte aligned rows)
 

@@ -68,6 +68,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return true;
 }
 
+// Spinning variant of mbar_wait for waits on the critical path: polls with the non-blocking
+// test (no suspend, so no wake-up delay), checking the time bound every 64 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  if (timeout_ns == 0) return false;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (global_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// One lane of the (converged) warp is elected: the issue sites of tcgen05.mma run on whole
+// warps so that their operands stay warp-uniform, and only the elected lane issues.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\telect.sync rx|px, %1;\n\tselp.u32 %0, 1, 0, px;\n\t}"
+      : "=r"(p)
+      : "r"(0xffffffffu));
+  return p != 0;
+}
+
 // Programmatic dependent launch: a primary grid lets its dependent grid start launching; the
 // dependent waits for the primary grid's completion (and memory) before reading its results.
 // Both are no-ops for grids launched without the programmatic-serialization attribute.
@@ -176,6 +201,16 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// As mma_bf16 with A read from TMEM: M rows = TMEM lanes, each 32-bit column holds two
+// consecutive K elements (the lower K index in the low half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // As mma_tf32 with A (M rows = TMEM lanes, one 32-bit column per K element) read from TMEM.
