@@ -12,6 +12,8 @@ Functions and the passages they follow:
   Prefix Caching for Hybrid LLMs", section 2 Eq. (1) and section 3 Eq. (2):
   token loop of the GDN update from S0 (zero by default) over each tail, with
   the readout o_t = S_t (scale q_t).
+  With ``scalar_decay``: the Mamba-2 family that the LinearKV page sets beside
+  GDN (scalar per-token transition), S_t = alpha_t S_{t-1} + beta_t v_t k_t^T.
 * :func:`chunk_operator` -- "LinearKV: One Cached State Suffices for
   Position-Independent Caching in Hybrid LLMs", composition passage: T_C as
   the product of the chunk's per-token transitions (latest on the left) and
@@ -50,6 +52,7 @@ class _Dims(ctypes.Structure):
         ("l2norm_qk", ctypes.c_int32),
         ("n_threads", ctypes.c_int32),
         ("scale", ctypes.c_double),
+        ("scalar_decay", ctypes.c_int32),
     ]
 
 
@@ -102,17 +105,18 @@ def num_threads(requested: int = 0) -> int:
 
 
 def replay(q, k, v, g, beta, cu_seqlens, S0=None, *, l2norm_qk=True, scale=1.0, want_O=True,
-           sel=None, n_threads=0):
+           sel=None, n_threads=0, scalar_decay=False):
     """Token-loop replay.  Shapes: q,k [T,h_k,d_k]; v [T,h_v,d_v]; g,beta [T,h_v];
     cu_seqlens [n+1]; S0 [n,h_v,d_v,d_k] or None.  ``sel``: optional list of
-    (sequence, v-head) pairs to compute (others stay zero).  Returns (S, O) in
-    fp64; O is None when ``want_O`` is False."""
+    (sequence, v-head) pairs to compute (others stay zero).  ``scalar_decay``:
+    the Mamba-2 family's scalar transition T_t = alpha_t I instead of GDN's.
+    Returns (S, O) in fp64; O is None when ``want_O`` is False."""
     q, k, v, g, beta, S0 = map(_f64, (q, k, v, g, beta, S0))
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
     T, h_k, d_k = k.shape
     h_v, d_v = v.shape[1], v.shape[2]
     n = cu.shape[0] - 1
-    dims = _Dims(n, h_k, h_v, d_k, d_v, int(bool(l2norm_qk)), int(n_threads), float(scale))
+    dims = _Dims(n, h_k, h_v, d_k, d_v, int(bool(l2norm_qk)), int(n_threads), float(scale), int(bool(scalar_decay)))
     S = np.zeros((n, h_v, d_v, d_k), dtype=np.float64)
     O = np.zeros((T, h_v, d_v), dtype=np.float64) if want_O else None
     sel_arr = None
@@ -127,7 +131,7 @@ def replay(q, k, v, g, beta, cu_seqlens, S0=None, *, l2norm_qk=True, scale=1.0, 
     return S, O
 
 
-def chunk_operator(k, g, beta, v, cu_seqlens, *, h_k=None, l2norm_qk=True, n_threads=0):
+def chunk_operator(k, g, beta, v, cu_seqlens, *, h_k=None, l2norm_qk=True, n_threads=0, scalar_decay=False):
     """(T_C, S_local) per chunk (sequence of cu_seqlens) and v-head.
     Returns T [n,h_v,d_k,d_k] and S_local [n,h_v,d_v,d_k], fp64."""
     k, g, beta, v = map(_f64, (k, g, beta, v))
@@ -135,7 +139,7 @@ def chunk_operator(k, g, beta, v, cu_seqlens, *, h_k=None, l2norm_qk=True, n_thr
     _, hk, d_k = k.shape
     h_v, d_v = v.shape[1], v.shape[2]
     n = cu.shape[0] - 1
-    dims = _Dims(n, hk, h_v, d_k, d_v, int(bool(l2norm_qk)), int(n_threads), 1.0)
+    dims = _Dims(n, hk, h_v, d_k, d_v, int(bool(l2norm_qk)), int(n_threads), 1.0, int(bool(scalar_decay)))
     Tc = np.zeros((n, h_v, d_k, d_k), dtype=np.float64)
     Sl = np.zeros((n, h_v, d_v, d_k), dtype=np.float64)
     rc = _load().gdn_oracle_chunk_operator(ctypes.byref(dims), _ptr(k), _ptr(g), _ptr(beta), _ptr(v),
@@ -151,7 +155,7 @@ def compose(T, S_local, S_in=None, *, n_threads=0):
     T, S_local, S_in = map(_f64, (T, S_local, S_in))
     K, h, d_k, _ = T.shape
     d_v = S_local.shape[2]
-    dims = _Dims(1, h, h, d_k, d_v, 0, int(n_threads), 1.0)
+    dims = _Dims(1, h, h, d_k, d_v, 0, int(n_threads), 1.0, 0)
     out = np.zeros((h, d_v, d_k), dtype=np.float64)
     rc = _load().gdn_oracle_compose(ctypes.byref(dims), K, _ptr(T), _ptr(S_local), _ptr(S_in), _ptr(out))
     if rc != 0:

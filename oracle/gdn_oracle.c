@@ -31,6 +31,13 @@
  * Optional per-token L2 normalisation of q and k (a flag): x / sqrt(sum x^2 + 1e-6),
  * applied before use, in fp64.
  *
+ * Scalar-decay family (a flag): the LinearKV page sets beside GDN the Mamba-2
+ * family, whose per-token transition is a scalar, so a chunk's transition is a
+ * single scalar decay.  Reading: T_t = alpha_t I, i.e. the same update without
+ * the rank-1 projection term,
+ *     S_i = alpha_i S_{i-1} + beta_i v_i k_i^T,
+ * with the same readout; its chunk transition is (prod alpha_t) I.
+ *
  * Everything is fp64; inputs arrive already widened to fp64 by the caller.
  * Threads split independent (sequence, head) problems only; each problem is
  * the plain token loop.
@@ -51,6 +58,7 @@ typedef struct {
   int32_t l2norm_qk;/* 1: normalise q and k per (token, head) before use */
   int32_t n_threads;/* 0: all online cores */
   double scale;     /* multiplies q in the readout */
+  int32_t scalar_decay; /* 1: Mamba-2 family, scalar per-token transition T_t = alpha_t I */
 } gdn_oracle_dims;
 
 /* ------------------------------------------------------------------ */
@@ -153,7 +161,8 @@ static void replay_one(const gdn_oracle_dims* d, const double* q, const double* 
     }
     for (int64_t i = 0; i < dv; ++i) {
       for (int64_t j = 0; j < dk; ++j) {
-        S[i * dk + j] = alpha * S[i * dk + j] - alpha * b * sk[i] * kt[j] + b * vt[i] * kt[j];
+        S[i * dk + j] = d->scalar_decay ? alpha * S[i * dk + j] + b * vt[i] * kt[j]
+                                        : alpha * S[i * dk + j] - alpha * b * sk[i] * kt[j] + b * vt[i] * kt[j];
       }
     }
     if (O) {
@@ -214,6 +223,7 @@ int gdn_oracle_replay(const gdn_oracle_dims* d, const double* q, const double* k
  *   Tc <- T_t Tc,   T_t = alpha_t (I - beta_t k_t k_t^T),
  * where T_t Tc is evaluated from T_t's definition as
  *   alpha_t (Tc - beta_t k_t (k_t^T Tc)).
+ * Scalar-decay family: T_t = alpha_t I, so Tc <- alpha_t Tc.
  */
 static void transition_product(const gdn_oracle_dims* d, const double* k, const double* g,
                                const double* beta, int64_t t0, int64_t t1, int64_t hv, double* Tc) {
@@ -236,7 +246,7 @@ static void transition_product(const gdn_oracle_dims* d, const double* k, const 
     }
     for (int64_t i = 0; i < dk; ++i)
       for (int64_t j = 0; j < dk; ++j)
-        Tc[i * dk + j] = alpha * (Tc[i * dk + j] - b * kt[i] * ktT[j]);
+        Tc[i * dk + j] = d->scalar_decay ? alpha * Tc[i * dk + j] : alpha * (Tc[i * dk + j] - b * kt[i] * ktT[j]);
   }
   free(kt); free(ktT);
 }

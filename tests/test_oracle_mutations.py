@@ -29,6 +29,9 @@ MUTATIONS = {
     "compose_product_reversed": ("matmul(prod, Tm, tmp, dk, dk, dk);", "matmul(Tm, prod, tmp, dk, dk, dk);"),
     "compose_drops_entering_state": ("(c->S_in ? 0 : 1)", "1"),
     "norm_skipped_on_query": ("l2_normalise(qin, dk, qt);", "memcpy(qt, qin, sizeof(double) * (size_t)dk);"),
+    "scalar_family_keeps_projection": ("d->scalar_decay ? alpha * S[i * dk + j] + b * vt[i] * kt[j]",
+                                       "d->scalar_decay ? alpha * S[i * dk + j] - alpha * b * sk[i] * kt[j] + b * vt[i] * kt[j]"),
+    "scalar_family_transition_undecayed": ("d->scalar_decay ? alpha * Tc[i * dk + j]", "d->scalar_decay ? Tc[i * dk + j]"),
 }
 
 

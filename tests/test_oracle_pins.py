@@ -339,3 +339,66 @@ def test_rel_err_on_hand_computed_vectors():
     # float32 inputs are compared in fp64 (the difference is not rounded away)
     a32 = np.float32(1.0) + np.float32(2 ** -20)
     assert oracle.rel_err(np.array([a32], np.float32), np.array([1.0], np.float32)) == 2 ** -20
+
+
+# ---------------------------------------------------------------- the scalar-decay (Mamba-2) family
+
+def test_scalar_decay_closed_form():
+    """The LinearKV page's other recurrence family has a scalar per-token transition, so the
+    state is a decayed sum: S_T = (prod alpha) S0 + sum_t (prod_{s>t} alpha_s) beta_t v_t k_t^T,
+    and o_t = S_t q_t reads the state right after token t."""
+    rng = _rng(70)
+    T, dk, dv = 11, 5, 4
+    q, k = rng.standard_normal((T, 1, dk)), rng.standard_normal((T, 1, dk))
+    v = rng.standard_normal((T, 1, dv))
+    g = -rng.uniform(0.0, 0.6, size=(T, 1))
+    beta = rng.uniform(0.1, 1.0, size=(T, 1))
+    S0 = rng.standard_normal((1, 1, dv, dk))
+    S, O = oracle.replay(q, k, v, g, beta, [0, T], S0, l2norm_qk=False, scalar_decay=True)
+    G = np.cumsum(g[:, 0])
+    for t in range(T):
+        St = np.exp(G[t]) * S0[0, 0]
+        for s in range(t + 1):
+            St = St + np.exp(G[t] - G[s]) * beta[s, 0] * np.outer(v[s, 0], k[s, 0])
+        np.testing.assert_allclose(O[t, 0], St @ q[t, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S[0, 0], St, rtol=1e-12, atol=1e-12)
+
+
+def test_scalar_decay_brute_force_and_difference_from_gdn():
+    """Dense left-form product with T_t = alpha_t I on the transposed state matches; and the same
+    inputs under GDN differ exactly by the projection term (a scalar model keeps the k direction
+    of the old state, GDN's delta rule removes it)."""
+    rng = _rng(71)
+    T, dk, dv = 6, 4, 3
+    q, k = rng.standard_normal((T, 1, dk)), _unit(rng, (T, 1, dk))
+    v = rng.standard_normal((T, 1, dv))
+    g = -rng.uniform(0.0, 0.3, size=(T, 1))
+    beta = rng.uniform(0.2, 0.9, size=(T, 1))
+    S, _ = oracle.replay(q, k, v, g, beta, [0, T], None, l2norm_qk=False, scalar_decay=True)
+    St = np.zeros((dk, dv))  # the pages' left form acts on S^T
+    for t in range(T):
+        Tt = np.exp(g[t, 0]) * np.eye(dk)
+        St = Tt @ St + beta[t, 0] * np.outer(k[t, 0], v[t, 0])
+    np.testing.assert_allclose(S[0, 0], St.T, rtol=1e-12, atol=1e-12)
+    # one token on a known state: scalar keeps S0 k, GDN subtracts beta (S0 k) k^T
+    S0 = rng.standard_normal((1, 1, dv, dk))
+    a = np.exp(g[:1])
+    Ss, _ = oracle.replay(q[:1], k[:1], v[:1], g[:1], beta[:1], [0, 1], S0, l2norm_qk=False, scalar_decay=True)
+    Sg, _ = oracle.replay(q[:1], k[:1], v[:1], g[:1], beta[:1], [0, 1], S0, l2norm_qk=False)
+    proj = a[0, 0] * beta[0, 0] * np.outer(S0[0, 0] @ k[0, 0], k[0, 0])
+    np.testing.assert_allclose(Ss[0, 0] - Sg[0, 0], proj, rtol=1e-12, atol=1e-12)
+
+
+def test_scalar_decay_chunk_transition_is_a_scalar_and_composition_is_exact():
+    """T_C = (prod alpha) I for the scalar family, and composing isolated chunks' operators
+    equals the sequential replay of all their tokens."""
+    x = synthetic.make_replay_inputs([7, 5, 9], 1, 2, 6, 4, dtype="f32", seed=72, gate_scale=0.5)
+    Tc, Sl = oracle.chunk_operator(x.k, x.g, x.beta, x.v, x.cu_seqlens, scalar_decay=True)
+    cu = x.cu_seqlens
+    for c in range(3):
+        for h in range(2):
+            prod = np.exp(np.sum(x.g[cu[c]:cu[c + 1], h].astype(np.float64)))
+            np.testing.assert_allclose(Tc[c, h], prod * np.eye(6), rtol=1e-13, atol=1e-15)
+    S_comp = oracle.compose(Tc, Sl)
+    S_seq, _ = oracle.replay(x.q, x.k, x.v, x.g, x.beta, [0, int(cu[-1])], want_O=False, scalar_decay=True)
+    np.testing.assert_allclose(S_comp, S_seq[0], rtol=1e-12, atol=1e-13)
