@@ -336,6 +336,198 @@ def measure_rows(dev, flush, peaks, replay_us):
                        "path": "tcgen05 tensor cores, split tf32 (fp32 accuracy)" if x.d_k == 128 and x.d_v == 128
                        else "fp32 CUDA cores"}
     api.gdn_get_status()
+    rows |= measure_more_rows(dev, flush, peaks, dev_inputs)
+    return rows
+
+
+def measure_more_rows(dev, flush, peaks, dev_inputs):
+    """Short tail and tiny workloads, all 48 varlen layers, the replay-error curve over the replay
+    ratio, copy-stream overlap with a synthetic FA KV upload, and the last-block initializer."""
+    import torch
+
+    from gated_deltanet_state_chunked_gb300 import api, synthetic
+    import oracle
+
+    rows = {}
+    hbm, bf16 = peaks["hbm_gbs"], peaks["bf16_tflops"]
+
+    def replay_row(name, state_only=False, reps=10):
+        x = synthetic.workload_inputs(name)
+        d = dev_inputs(x)
+        dt = torch.bfloat16 if x.dtype == "bf16" else torch.float32
+        O = None if state_only else torch.empty((x.total_tokens, x.h_v, x.d_v), dtype=dt, device=dev)
+        S = torch.empty((x.n_seqs, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        us = _timed_us(lambda: api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], O_out=O, S_out=S,
+                                              state_only=state_only), flush, reps)
+        fl, by = algorithmic(x, with_O=not state_only)
+        S_ref, _ = oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, want_O=False,
+                                 sel=[(0, 0), (0, x.h_v - 1)])
+        Sh = S.double().cpu().numpy()
+        err = max(oracle.rel_err(Sh[0, h], S_ref[0, h]) for h in (0, x.h_v - 1))
+        return {"tokens": x.total_tokens, "heads": x.h_v, "d": x.d_k, "dtype": x.dtype, "state_only": state_only,
+                "us": us, "tokens_per_s": x.total_tokens / (us * 1e-6), "algorithmic_bytes": by,
+                "algorithmic_flops": fl, "hbm_frac": by / (us * 1e-6) / 1e9 / hbm,
+                "tensor_frac": fl / (us * 1e-6) / 1e12 / bf16, "rel_err_S_sampled": err}
+
+    rows["layer_r1638"] = replay_row("layer_r1638")
+    rows["layer_r1638_state_only"] = replay_row("layer_r1638", state_only=True)
+    rows["layer_r3277_state_only"] = replay_row("layer_r3277", state_only=True)
+    rows["tiny"] = replay_row("tiny", reps=20)
+
+    # 48 stacked independent layers of 64 concurrent tails: each layer its own tail lengths (from
+    # the seed, as in the tests) and its own inputs, drawn on the GPU with the same distributions
+    # (generating 48 x 1.6 GB on the host would take minutes); one call per layer, each timed.
+    lay_us, lay_tok = [], []
+    g = torch.Generator(device=dev)
+    for layer in range(48):
+        seed = synthetic.config_seed(2, layer)
+        lens = synthetic.varlen_tail_lengths(64, seed)
+        T = int(sum(lens))
+        g.manual_seed(seed)
+        unit = lambda shape: torch.nn.functional.normalize(torch.randn(shape, generator=g, device=dev), dim=-1)
+        q, k = unit((T, 16, 128)).to(torch.bfloat16), unit((T, 16, 128)).to(torch.bfloat16)
+        v = torch.randn((T, 32, 128), generator=g, device=dev).to(torch.bfloat16)
+        beta = torch.sigmoid(torch.randn((T, 32), generator=g, device=dev))
+        gg = -torch.nn.functional.softplus(torch.randn((T, 32), generator=g, device=dev) + 2.0) * 0.1
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device=dev)
+        O = torch.empty((T, 32, 128), dtype=torch.bfloat16, device=dev)
+        S = torch.empty((64, 32, 128, 128), dtype=torch.float32, device=dev)
+        lay_us.append(_timed_us(lambda: api.gdn_replay(q, k, v, gg, beta, cu, O_out=O, S_out=S), flush, 2, warmup=1))
+        lay_tok.append(T)
+        del q, k, v, beta, gg, O, S
+    tot_us = float(sum(lay_us))
+    rows["varlen_48_layers"] = {"layers": 48, "tails_per_layer": 64, "tokens_total": int(sum(lay_tok)),
+                                "us_total": tot_us, "us_per_layer_mean": tot_us / 48,
+                                "us_per_layer_min": float(min(lay_us)), "us_per_layer_max": float(max(lay_us)),
+                                "tokens_per_s_per_layer": float(sum(lay_tok)) / (tot_us * 1e-6),
+                                "inputs": "values drawn on the GPU (torch.Generator, seeded per layer) with the "
+                                          "workload's distributions; tail lengths from the seed"}
+
+    # replay error against the full-prefix state over the replay ratio (32K prefix; weak-decay
+    # gates make the dropped prefix state matter, the workload gates make it vanish)
+    curve = {}
+    for tag, gs in (("weak_decay", 1e-3), ("workload_gates", 0.1)):
+        x = synthetic.workload_inputs("full_32k", gate_scale=gs)
+        d = dev_inputs(x)
+        S_full = torch.empty((1, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], S_out=S_full, state_only=True)
+        pts = []
+        for rho in (0.01, 0.02, 0.05, 0.10, 0.20):
+            r = synthetic.tail_length(x.total_tokens, rho)
+            tail = {n: d[n][-r:].contiguous() for n in ("q", "k", "v", "g", "beta")}
+            S_t = torch.empty_like(S_full)
+            api.gdn_replay(tail["q"], tail["k"], tail["v"], tail["g"], tail["beta"],
+                           torch.tensor([0, r], dtype=torch.int32, device=dev), S_out=S_t, state_only=True)
+            torch.cuda.synchronize()
+            pts.append({"rho": rho, "tail_tokens": r,
+                        "rel_err_S": oracle.rel_err(S_t.double().cpu().numpy(), S_full.double().cpu().numpy())})
+        curve[tag] = pts
+        del d
+    rows["replay_error_vs_rho"] = {"prefix_tokens": 32768, "points": curve}
+
+    # copy-stream overlap: a synthetic FA KV upload of the matched prefix (one full-attention
+    # layer: 32768 tokens x 8 KV heads x 128 x (K, V), bf16 = 128 MiB) from pinned host memory,
+    # serialised with one GDN layer's replay on one stream, then on a second stream beside it.
+    x = synthetic.workload_inputs("layer_r3277")
+    d = dev_inputs(x)
+    O = torch.empty((x.total_tokens, x.h_v, x.d_v), dtype=torch.bfloat16, device=dev)
+    S = torch.empty((1, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    kv_bytes = 32768 * 8 * 128 * 2 * 2
+    h_kv = torch.empty(kv_bytes, dtype=torch.uint8).pin_memory()
+    d_kv = torch.empty(kv_bytes, dtype=torch.uint8, device=dev)
+    s_main, s_copy = torch.cuda.current_stream(dev), torch.cuda.Stream(dev)
+    replay = lambda st: api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], O_out=O, S_out=S, stream=st)
+
+    def timed(fn, reps=5):
+        ts = []
+        for _ in range(reps + 1):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_main)
+            fn()
+            e1.record(s_main)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return float(np.median(ts[1:]))
+
+    def copy_only():
+        d_kv.copy_(h_kv, non_blocking=True)
+
+    def serialised():
+        d_kv.copy_(h_kv, non_blocking=True)
+        replay(s_main)
+
+    def overlapped():
+        ev = torch.cuda.Event()
+        ev.record(s_main)
+        s_copy.wait_event(ev)
+        with torch.cuda.stream(s_copy):
+            d_kv.copy_(h_kv, non_blocking=True)
+        replay(s_main)
+        done = torch.cuda.Event()
+        done.record(s_copy)
+        s_main.wait_event(done)
+
+    t_copy, t_rep = timed(copy_only), timed(lambda: replay(s_main))
+    t_ser, t_ovl = timed(serialised), timed(overlapped)
+    rows["copy_overlap"] = {"fa_kv_bytes": kv_bytes, "copy_us": t_copy, "replay_us": t_rep,
+                            "serialised_us": t_ser, "overlapped_us": t_ovl,
+                            "hidden_us": t_copy + t_rep - t_ovl, "h2d_gbs": kv_bytes / (t_copy * 1e-6) / 1e9,
+                            "fa_kv": "one full-attention layer: 32768 tokens x 8 KV heads x 128 x (K, V), bf16, pinned host"}
+    del h_kv, d_kv, d
+
+    # LinearKV's last-block initializer (the last chunk's local state alone) against the exact
+    # composition of all chunk operators and against sequential replay of all chunks, on 16
+    # isolated 2048-token chunks (workload gates, then weak decay)
+    lb = {}
+    for fam, scalar in (("gdn", False), ("scalar_decay", True)):
+        for tag, wd in (("workload_gates", False), ("weak_decay", True)):
+            x = synthetic.chunk_workload_inputs(weak_decay=wd)
+            d = dev_inputs(x)
+            K = x.n_seqs
+            T = torch.empty((K, x.h_v, x.d_k, x.d_k), dtype=torch.float32, device=dev)
+            Sl = torch.empty((K, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+            api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], d["cu"], T_out=T, Slocal_out=Sl,
+                                   scalar_decay=scalar)
+            SK = api.gdn_compose([T[j] for j in range(K)], [Sl[j] for j in range(K)])
+            S_seq = torch.empty((1, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+            cu_all = torch.tensor([0, x.total_tokens], dtype=torch.int32, device=dev)
+            api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_all, S_out=S_seq, state_only=True,
+                           precise=True, scalar_decay=scalar)
+            torch.cuda.synchronize()
+            ref = S_seq[0].double().cpu().numpy()
+            lb[f"{fam}_{tag}"] = {"exact_composition_rel_err": oracle.rel_err(SK.double().cpu().numpy(), ref),
+                                  "last_block_rel_err": oracle.rel_err(Sl[K - 1].double().cpu().numpy(), ref)}
+            del d
+    rows["last_block_initializer"] = {"chunks": 16, "chunk_tokens": 2048, "heads": 32,
+                                      "vs": "sequential replay of all chunks (fp32 path)",
+                                      "families": "gdn: dense rank-1 transitions; scalar_decay: Mamba-2 scalar transitions",
+                                      "cases": lb}
+
+    # chunk-operator parallel scan: the 3277-token tail split into G segments whose operators are
+    # built side by side (fp32 chunk-operator path), then composed, against the sequential replay
+    x = synthetic.workload_inputs("layer_r3277")
+    d = dev_inputs(x)
+    S_seq = torch.empty((1, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    seq_us = _timed_us(lambda: api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], S_out=S_seq,
+                                              state_only=True), flush, 5)
+    ps = {"sequential_state_only_us": seq_us, "segments": []}
+    for G in (2, 4, 8):
+        edges = [round(i * x.total_tokens / G) for i in range(G + 1)]
+        cu_g = torch.tensor(edges, dtype=torch.int32, device=dev)
+        T = torch.empty((G, x.h_v, x.d_k, x.d_k), dtype=torch.float32, device=dev)
+        Sl = torch.empty((G, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        SK = torch.empty((x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        op = lambda: api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], cu_g, T_out=T, Slocal_out=Sl)
+        comp = lambda: api.gdn_compose([T[j] for j in range(G)], [Sl[j] for j in range(G)], S_out=SK)
+        op_us, comp_us = _timed_us(op, flush, 3, warmup=1), _timed_us(comp, flush, 5)
+        torch.cuda.synchronize()
+        ps["segments"].append({"G": G, "chunk_operators_us": op_us, "compose_us": comp_us, "total_us": op_us + comp_us,
+                               "rel_err_vs_sequential": oracle.rel_err(SK.double().cpu().numpy(),
+                                                                       S_seq[0].double().cpu().numpy())})
+    rows["parallel_scan_replay"] = ps
+    del d
+    api.gdn_get_status()
     return rows
 
 
@@ -507,9 +699,28 @@ def run_ours(args):
         e2e_ms = e2e_run(args.steps) / args.steps
         api.gdn_get_status()
         e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+        # One call alone, not pipelined: upload, replay, read-back on one stream (the latency a
+        # cache hit waits for when nothing else is in flight).
+        def latency_once():
+            (dbuf, (dq, dk, dv, dg, db, dcu)), (obuf, (dO, dS)) = dins[0], douts[0]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            dbuf.copy_(hin, non_blocking=True)
+            api.gdn_replay(dq, dk, dv, dg, db, dcu, None, O_out=dO, S_out=dS, precise=args.precise, stream=stream)
+            hout[0][0].copy_(obuf, non_blocking=True)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+            return t0.elapsed_time(t1)
+
+        for _ in range(3):
+            latency_once()
+        lat_ms = float(np.median([latency_once() for _ in range(max(5, args.steps))]))
+        api.gdn_get_status()
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "pipelining": f"{NB} streams, {NB} buffer sets: uploads of later steps overlap a step's replay and read-back; one copy per direction per step"}
+               "pipelining": f"{NB} streams, {NB} buffer sets: uploads of later steps overlap a step's replay and read-back; one copy per direction per step",
+               "latency_ms_one_call": lat_ms,
+               "latency": "one call alone on one stream: one upload of the packed inputs from pinned memory, the replay, one read-back of O and S"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

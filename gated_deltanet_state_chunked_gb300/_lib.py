@@ -23,6 +23,7 @@ GDN_BF16 = 1
 GDN_QK_L2NORM = 1
 GDN_STATE_ONLY = 2
 GDN_PRECISE = 4
+GDN_SCALAR_DECAY = 8
 
 ERROR_NAMES = {
     GDN_ERR_ARG: "GDN_ERR_ARG", GDN_ERR_SHAPE: "GDN_ERR_SHAPE", GDN_ERR_ALIGN: "GDN_ERR_ALIGN",

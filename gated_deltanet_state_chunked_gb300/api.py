@@ -40,7 +40,7 @@ def _need_cuda(name, t, dtype=None, shape=None):
 
 
 def gdn_replay(q, k, v, g, beta, cu_seqlens, S0=None, *, O_out=None, S_out=None, l2norm_qk=True,
-               scale=1.0, state_only=False, precise=False, stream=None):
+               scale=1.0, state_only=False, precise=False, scalar_decay=False, stream=None):
     """Rebuild the recurrent state of each packed replay tail (see gdn.h).
 
     q, k: [T, h_k, d_k]; v: [T, h_v, d_v] (all bf16 or all fp32); g, beta: fp32
@@ -71,7 +71,7 @@ def gdn_replay(q, k, v, g, beta, cu_seqlens, S0=None, *, O_out=None, S_out=None,
     else:
         O_out = None
     flags = (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_STATE_ONLY if state_only else 0) \
-        | (_lib.GDN_PRECISE if precise else 0)
+        | (_lib.GDN_PRECISE if precise else 0) | (_lib.GDN_SCALAR_DECAY if scalar_decay else 0)
     dims = _lib.GdnDims(n, T, h_k, h_v, d_k, d_v, _DTYPE[dt], flags, float(scale))
     rc = lib.gdn_replay(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
                         _ptr(S0), _ptr(O_out), _ptr(S_out), _stream_handle(stream, k.device))
@@ -80,7 +80,7 @@ def gdn_replay(q, k, v, g, beta, cu_seqlens, S0=None, *, O_out=None, S_out=None,
 
 
 def gdn_replay_noalloc(q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, *, l2norm_qk=True, scale=1.0,
-                       state_only=False, precise=False, stream=None):
+                       state_only=False, precise=False, scalar_decay=False, stream=None):
     """gdn_replay for callers that cannot allocate device memory at call time.
 
     Same arguments and results as gdn_replay, except that the outputs O_out
@@ -110,7 +110,7 @@ def gdn_replay_noalloc(q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, *, l2norm
     else:
         O_out = None
     flags = (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_STATE_ONLY if state_only else 0) \
-        | (_lib.GDN_PRECISE if precise else 0)
+        | (_lib.GDN_PRECISE if precise else 0) | (_lib.GDN_SCALAR_DECAY if scalar_decay else 0)
     dims = _lib.GdnDims(n, T, h_k, h_v, d_k, d_v, _DTYPE[dt], flags, float(scale))
     rc = lib.gdn_replay_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                 _ptr(cu_seqlens), _ptr(S0), _ptr(O_out), _ptr(S_out), _stream_handle(stream, k.device))
@@ -119,8 +119,9 @@ def gdn_replay_noalloc(q, k, v, g, beta, cu_seqlens, S0, O_out, S_out, *, l2norm
 
 
 def gdn_chunk_operator(k, g, beta, v, cu_seqlens=None, *, T_out=None, Slocal_out=None, l2norm_qk=True,
-                       stream=None):
+                       scalar_decay=False, stream=None):
     """(T_C, S_local) of each chunk (range of cu_seqlens, or all tokens when None).
+    ``scalar_decay``: the scalar-transition family (T_C is then a scaled identity).
     Returns T fp32 [n, h_v, d_k, d_k] and S_local fp32 [n, h_v, d_v, d_k]."""
     lib = _lib.load()
     T, h_k, d_k = k.shape
@@ -140,7 +141,7 @@ def gdn_chunk_operator(k, g, beta, v, cu_seqlens=None, *, T_out=None, Slocal_out
         Slocal_out = torch.empty((n, h_v, d_v, d_k), dtype=torch.float32, device=k.device)
     _need_cuda("T_out", T_out, torch.float32, (n, h_v, d_k, d_k))
     _need_cuda("Slocal_out", Slocal_out, torch.float32, (n, h_v, d_v, d_k))
-    flags = _lib.GDN_QK_L2NORM if l2norm_qk else 0
+    flags = (_lib.GDN_QK_L2NORM if l2norm_qk else 0) | (_lib.GDN_SCALAR_DECAY if scalar_decay else 0)
     dims = _lib.GdnDims(n, T, h_k, h_v, d_k, d_v, _DTYPE[dt], flags, 1.0)
     rc = lib.gdn_chunk_operator(ctypes.byref(dims), _ptr(k), _ptr(g), _ptr(beta), _ptr(v), _ptr(cu_seqlens),
                                 _ptr(T_out), _ptr(Slocal_out), _stream_handle(stream, k.device))

@@ -47,7 +47,8 @@ int check_head_dims(const gdn_dims* d) {
 int check_token_dims(const gdn_dims* d) {
   if (d->n_seqs < 0 || d->total_tokens < 0) return fail(GDN_ERR_ARG, "negative n_seqs or total_tokens");
   if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "dtype %d", d->dtype);
-  if (d->flags & ~(GDN_QK_L2NORM | GDN_STATE_ONLY | GDN_PRECISE)) return fail(GDN_ERR_ARG, "unknown flag bits 0x%x", d->flags);
+  if (d->flags & ~(GDN_QK_L2NORM | GDN_STATE_ONLY | GDN_PRECISE | GDN_SCALAR_DECAY))
+    return fail(GDN_ERR_ARG, "unknown flag bits 0x%x", d->flags);
   return check_head_dims(d);
 }
 
@@ -112,6 +113,7 @@ int check_replay_args(const gdn_dims* dims, const void* q, const void* k, const 
   p->h_k = dims->h_k; p->h_v = dims->h_v; p->d_k = dims->d_k; p->d_v = dims->d_v;
   p->augmented = 0; p->l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
   p->write_O = state_only ? 0 : 1; p->scale = dims->scale; p->status = status;
+  p->scalar_decay = (dims->flags & GDN_SCALAR_DECAY) ? 1 : 0;
   return GDN_OK;
 }
 
@@ -220,6 +222,7 @@ int gdn_chunk_operator(const gdn_dims* dims, const void* k, const float* g, cons
   p.h_k = dims->h_k; p.h_v = dims->h_v; p.d_k = dims->d_k; p.d_v = dims->d_v;
   p.augmented = 1; p.l2norm = (dims->flags & GDN_QK_L2NORM) ? 1 : 0;
   p.write_O = 0; p.scale = 1.f; p.status = status;
+  p.scalar_decay = (dims->flags & GDN_SCALAR_DECAY) ? 1 : 0;
   // Two passes: the chunk-shared quantities once per (chunk, v-head) into pool scratch, then the
   // row slices of the augmented state [S; P] read them.
   const cudaStream_t st = static_cast<cudaStream_t>(stream);

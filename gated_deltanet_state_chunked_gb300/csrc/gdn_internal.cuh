@@ -27,6 +27,7 @@ struct SimtParams {
   int augmented;  // 1: state carries d_k extra transition rows (chunk operator)
   int l2norm;
   int write_O;
+  int scalar_decay;  // 1: scalar per-token transition (no rank-1 projection term)
   float scale;
   int* status;    // sticky device status word
   unsigned char* rec;  // optional per-(chunk, v-head) records of the chunk-shared quantities (scratch)

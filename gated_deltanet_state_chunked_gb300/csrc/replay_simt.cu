@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
       for (int j = 0; j < 4; ++j) {
         const int s = si + j;
         const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
-        sm.A[t * tcp::MST + s] = s < t ? sm.beta[t] * decay * akk[i][j] : 0.f;
+        sm.A[t * tcp::MST + s] = (s < t && !p.scalar_decay) ? sm.beta[t] * decay * akk[i][j] : 0.f;
         pv[j] = s <= t ? decay * aqk[i][j] : 0.f;
       }
       *reinterpret_cast<float4*>(rec + REC_P + t * C + si) = make_float4(pv[0], pv[1], pv[2], pv[3]);
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
         for (int j = 0; j < 4; ++j) {
           const int t = ti + i, s = si + j;
           const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
-          sm.A[t * GST + s] = s < t ? sm.beta[t] * decay * akk[i][j] : 0.f;
+          sm.A[t * GST + s] = (s < t && !p.scalar_decay) ? sm.beta[t] * decay * akk[i][j] : 0.f;
           sm.P[t * GST + s] = s <= t ? decay * aqk[i][j] : 0.f;
         }
     }
@@ -522,7 +522,8 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     // ---- R = diag(beta) (V - diag(gamma) X)   (in place in V)
     for (int i = tid; i < C * RS; i += NT) {
       const int t = i / RS, r = i % RS;
-      sm.V[t * VST + r] = sm.beta[t] * (sm.V[t * VST + r] - sm.gam[t] * sm.X[t * VST + r]);
+      // (scalar-decay family: no rank-1 projection, so no correction by the entering state)
+      sm.V[t * VST + r] = sm.beta[t] * (p.scalar_decay ? sm.V[t * VST + r] : sm.V[t * VST + r] - sm.gam[t] * sm.X[t * VST + r]);
     }
     __syncthreads();
 

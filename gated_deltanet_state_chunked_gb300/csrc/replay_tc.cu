@@ -76,6 +76,7 @@ struct PrepParams {
   unsigned char* rec;  // records [chunk][h_v]
   int* status;
   int n_seqs, total_tokens, h_k, h_v, l2norm, write_O;
+  int scalar_decay;  // 1: A = 0 (M = I) and W = 0 (no rank-1 projection term)
   float scale;
 };
 
@@ -315,6 +316,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 av[i] = s < t ? bt * exp2f(g_t - G2_[s]) * cRk[s] * kq[i] : 0.f;
               }
             }
+            if (p.scalar_decay) {  // scalar-decay family: no rank-1 projection, A = 0 and M = I
+#pragma unroll
+              for (int i = 0; i < 32; ++i) av[i] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
               *reinterpret_cast<float4*>(A_ + t * MST + half * 32 + i) = make_float4(av[i], av[i + 1], av[i + 2], av[i + 3]);
@@ -381,8 +386,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         const float4 b0 = *reinterpret_cast<const float4*>(gB + s), b1 = *reinterpret_cast<const float4*>(gB + s + 4);
         const float4 y0 = *reinterpret_cast<const float4*>(gGam + s), y1 = *reinterpret_cast<const float4*>(gGam + s + 4);
         const float4 r0 = *reinterpret_cast<const float4*>(cRk + s), r1 = *reinterpret_cast<const float4*>(cRk + s + 4);
-        const float wf[8] = {y0.x * r0.x, y0.y * r0.y, y0.z * r0.z, y0.w * r0.w,
-                             y1.x * r1.x, y1.y * r1.y, y1.z * r1.z, y1.w * r1.w};
+        // Mw = M diag(beta gamma rk); zero for the scalar-decay family (no correction W S0^T)
+        const float wz = p.scalar_decay ? 0.f : 1.f;
+        const float wf[8] = {wz * y0.x * r0.x, wz * y0.y * r0.y, wz * y0.z * r0.z, wz * y0.w * r0.w,
+                             wz * y1.x * r1.x, wz * y1.y * r1.y, wz * y1.z * r1.z, wz * y1.w * r1.w};
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int t = 16 * it + (gt >> 3);
@@ -1095,7 +1102,7 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   PrepParams pp;
   pp.g = p.g; pp.beta = p.beta; pp.cu = p.cu; pp.rec = rec; pp.status = p.status;
   pp.n_seqs = p.n_seqs; pp.total_tokens = p.total_tokens; pp.h_k = p.h_k; pp.h_v = p.h_v; pp.l2norm = p.l2norm;
-  pp.write_O = p.write_O; pp.scale = p.scale;
+  pp.write_O = p.write_O; pp.scale = p.scale; pp.scalar_decay = p.scalar_decay;
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepLay::ALLOC);
   if (e != cudaSuccess) return e;
   const long long items_ub = ((long long)(p.total_tokens + C - 1) / C + p.n_seqs) * p.h_k;

@@ -67,6 +67,14 @@ extern "C" {
 #define GDN_QK_L2NORM 1u   /* normalise q and k per (token, head): x / sqrt(sum x^2 + 1e-6) */
 #define GDN_STATE_ONLY 2u  /* rebuild the state only; O_out may be NULL and is not written */
 #define GDN_PRECISE 4u     /* bf16 inputs: take the fp32 CUDA-core path instead of the tensor-core path */
+/* Scalar-decay recurrence family (Mamba-2), which "LinearKV: One Cached State
+ * Suffices for Position-Independent Caching in Hybrid LLMs" (composition passage)
+ * sets beside GDN: the per-token transition is the scalar alpha_t instead of
+ * alpha_t (I - beta_t k_t k_t^T), i.e. S_t = alpha_t S_{t-1} + beta_t v_t k_t^T
+ * (beta_t scales the input; same readout), so a chunk's transition is
+ * (prod alpha_t) I.  Accepted by gdn_replay, gdn_replay_noalloc and
+ * gdn_chunk_operator (whose T_out is then that scaled identity). */
+#define GDN_SCALAR_DECAY 8u
 
 typedef struct {
   int32_t n_seqs;       /* packed sequences (replay tails, or chunks for gdn_chunk_operator) */
@@ -76,7 +84,7 @@ typedef struct {
   int32_t d_k;          /* key/query head dim: a multiple of 8, at most 128 */
   int32_t d_v;          /* value head dim: a multiple of 8, at most 128 */
   int32_t dtype;        /* GDN_F32 or GDN_BF16 */
-  uint32_t flags;       /* GDN_QK_L2NORM | GDN_STATE_ONLY | GDN_PRECISE */
+  uint32_t flags;       /* GDN_QK_L2NORM | GDN_STATE_ONLY | GDN_PRECISE | GDN_SCALAR_DECAY */
   float scale;          /* multiplies q in the readout (1.0 when unsure) */
 } gdn_dims;
 

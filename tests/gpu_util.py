@@ -21,9 +21,9 @@ def to_device(x, dev="cuda"):
     return out
 
 
-def oracle_replay(x, l2norm_qk=True, scale=1.0, want_O=True, sel=None):
+def oracle_replay(x, l2norm_qk=True, scale=1.0, want_O=True, sel=None, scalar_decay=False):
     return oracle.replay(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.S0, l2norm_qk=l2norm_qk, scale=scale,
-                         want_O=want_O, sel=sel)
+                         want_O=want_O, sel=sel, scalar_decay=scalar_decay)
 
 
 def host(t):

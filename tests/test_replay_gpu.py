@@ -218,3 +218,21 @@ def test_compose_wait_that_runs_out_reports_timeout_then_recovers(K):
     torch.cuda.synchronize()
     api.gdn_get_status()
     assert rel_err(host(out), oracle.compose(T, Sl, None)) <= TOL_F32
+
+
+def test_scalar_decay_family_fp32_and_chunk_operator():
+    """The scalar-transition (Mamba-2) family on the fp32 path, and its chunk operator: T_C is
+    (prod alpha) I and S_local matches the oracle."""
+    x = synthetic.make_replay_inputs([200, 1, 64, 129], 2, 4, 64, 32, dtype="f32", seed=15, with_S0=True,
+                                     gate_scale=1e-2)
+    O, S = _run(x, scalar_decay=True)
+    S_ref, O_ref = oracle_replay(x, scalar_decay=True)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+    assert rel_err(host(O), O_ref) <= TOL_F32
+    d = to_device(x)
+    T, Sl = api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], d["cu_seqlens"], scalar_decay=True)
+    torch.cuda.synchronize()
+    api.gdn_get_status()
+    T_ref, Sl_ref = oracle.chunk_operator(x.k, x.g, x.beta, x.v, x.cu_seqlens, scalar_decay=True)
+    assert rel_err(host(T), T_ref) <= TOL_F32
+    assert rel_err(host(Sl), Sl_ref) <= TOL_F32

@@ -175,3 +175,13 @@ def test_repeated_calls_are_deterministic():
     O1, S1 = _run(x)
     O2, S2 = _run(x)
     assert torch.equal(S1, S2) and torch.equal(O1, O2)
+
+
+@pytest.mark.parametrize("with_S0,gate_scale", [(False, 0.1), (True, 0.1), (True, 1e-3)])
+def test_scalar_decay_family(with_S0, gate_scale):
+    """The scalar-transition (Mamba-2) family on the tensor-core path: no rank-1 projection, so
+    the chunk's A and W vanish; ragged tails, an entering state, weak decay."""
+    x = synthetic.make_replay_inputs([300, 64, 1, 129], 2, 4, 128, 128, dtype="bf16", seed=311,
+                                     with_S0=with_S0, gate_scale=gate_scale)
+    O, S = _run(x, scalar_decay=True)
+    _check(x, O, S, scalar_decay=True)
