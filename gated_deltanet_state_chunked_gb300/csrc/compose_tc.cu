@@ -49,6 +49,9 @@ struct CTLay {
   static_assert(LB % 16 == 0 && TB % 16 == 0 && TROW % 16 == 0, "bulk copy alignment");
 };
 
+// Advance a shared-memory descriptor's start address by a byte offset (multiple of 16).
+__device__ __forceinline__ uint64_t dadd_bytes(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
@@ -63,7 +66,6 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BARS);  // MMAs of a step
   uint64_t* bar_ld = bar + 1;                                  // [2] copies of a step
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::BARS + 24);
-  volatile int* flag = reinterpret_cast<volatile int*>(sm + L::BARS + 28);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, hf = warp >> 2;
   const int h = blockIdx.y, row0 = blockIdx.x * CTR;
@@ -79,7 +81,6 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     mbar_init(&bar_ld[0], 1);
     mbar_init(&bar_ld[1], 1);
     mbar_fence_init();
-    *flag = 0;
     mbar_arrive_expect_tx(&bar_ld[0], L::STEP_BYTES);
     if (p.K > 1) mbar_arrive_expect_tx(&bar_ld[1], L::STEP_BYTES);
   }
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+  int timed_out = 0;  // this thread saw a bounded wait give up
   // copies of step s into buffer s & 1 (warps 4-7: one T row each, thread 128 also the slice);
   // the buffer's expect_tx was posted before the barrier that precedes this call
   auto issue_loads = [&](int s) {
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     if (r == 0) bulk_g2s(sm + L::LB + b * 16384, p.Slocal[s] + hoff + (size_t)row0 * CTD, 16384, &bar_ld[b]);
   };
   auto wait_ld = [&](int s) {
-    if (!mbar_wait(&bar_ld[s & 1], (uint32_t)((s >> 1) & 1), p.wait_ns)) *flag = 1;
+    if (!mbar_wait(&bar_ld[s & 1], (uint32_t)((s >> 1) & 1), p.wait_ns)) timed_out = 1;
   };
   // row m of T_s, columns [64 hf, 64 hf + 64), from its buffer -> tf32 hi and lo in TMEM
   auto store_T = [&](int s) {
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
 
   for (int j = 0; j < p.K; ++j) {
     // step j's MMAs done: S_j = D + S_local_j
-    if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) *flag = 1;
+    if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) timed_out = 1;
     tc_fence_after();
     float d[16], d2[16], d3[16], d4[16];
     tmem_ld16(tmem + lane_base + L::cD + 16 * hf, d);
@@ -220,9 +222,10 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     fence_async_smem();
     tc_fence_before();
     // buffer j & 1 is free once every thread has read S_local_j above (T_j went to TMEM a step ago)
-    if (tid == 0 && j + 2 < p.K) mbar_arrive_expect_tx(&bar_ld[j & 1], L::STEP_BYTES);
-    __syncthreads();
-    if (*flag) break;  // a wait gave up: issue nothing more (every thread reads the flag here)
+    // (only if this thread saw that phase complete: a pending phase takes no second arrival)
+    if (tid == 0 && j + 2 < p.K && !timed_out) mbar_arrive_expect_tx(&bar_ld[j & 1], L::STEP_BYTES);
+    // a wait that gave up in any thread stops the loop in every thread (the OR is taken by the barrier)
+    if (__syncthreads_or(timed_out)) break;
     if (issuer) issue();
     mma_step = j + 1;
     if (j + 2 < p.K) {
@@ -231,14 +234,16 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
     }
   }
   tc_fence_before();
-  __syncthreads();
-  if (*flag) {
+  if (__syncthreads_or(timed_out)) {
     // A wait gave up.  What was already issued still runs: let the copies in flight land before
     // the CTA's shared memory is released and the MMAs finish before the TMEM columns are (each
     // wait bounded at the default limit; a wait on a phase that has completed returns at once),
     // then report.
     if (tid == 0) {
-      for (int s = 0; s <= issued; ++s) mbar_wait(&bar_ld[s & 1], (uint32_t)((s >> 1) & 1), kWaitNs);
+      // the latest issued phase of each copy buffer (an earlier phase of the same buffer has
+      // completed, or the later one could not have been issued)
+      for (int s = issued > 0 ? issued - 1 : 0; s <= issued; ++s)
+        mbar_wait(&bar_ld[s & 1], (uint32_t)((s >> 1) & 1), kWaitNs);
       mbar_wait(bar, (uint32_t)(mma_step & 1), kWaitNs);
       atomicExch(p.status, GDN_ERR_TIMEOUT);
     }
@@ -249,11 +254,306 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
   if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Composition when the K operators T_1..T_K sit at one stride in memory (one array): every T_j
+// row is a row of one 2D view, so a step's T_j arrives by tensor copies (128 rows x 128 B boxes,
+// 128-byte swizzle), already in the layout of a K-major tensor-core operand.  The four CTAs of
+// a head form a cluster: each fetches one quarter (32 columns) of T_j and multicasts it to all
+// four, so T_j leaves L2 once per head instead of four times.  Per step:
+//   T_hi [S_lo | S_hi]  one product of N = 64, A = the T_j tile itself in shared memory (the
+//                       tensor core reads fp32 as tf32, dropping the low 13 mantissa bits);
+//   T_lo S_hi           N = 32, A = T - T_hi in TMEM (exact in fp32), accumulated into the S_hi
+//                       half of the same accumulator;
+// with K split over two accumulators (added by the epilogue in fp32).  T_lo of step j + 1 is
+// written into the other of two TMEM buffers while step j's MMAs run, so the serial chain per
+// step is the MMAs and the epilogue (D + S_local -> the split S tile).  T_j sits in one of three
+// shared-memory buffers, so copies run about two steps ahead; S_local_j is read into registers
+// at the top of step j, from L2, where it was prefetched when step j's copies were issued.
+//
+// Warps 0-7 prepare T_lo and run the epilogue; warp 8 issues the MMAs and owns the copies.
+// Copy protocol: after step j's MMAs complete, the CTA posts its
+// own expect_tx for step j + 3 and releases buffer j % 3 by arriving on the "free" barrier of
+// that buffer in all four CTAs; it issues its quarter of step j + 3 once its own free barrier has
+// all four arrivals.  Every CTA sees the same four arrivals, so a step is issued by all four or
+// by none, and a CTA that stops early (a bounded wait gave up) completes any step it released
+// before it leaves; a final cluster barrier keeps every CTA alive until its partners are done.
+// ---------------------------------------------------------------------------------------------
+constexpr int kComposeCluster = CTD / CTR;  // CTAs of one head
+constexpr int kTBufs = 3;                   // T_j buffers in shared memory
+constexpr int kMapThreads = CTNT + 32;      // 8 compute warps and the control warp
+
+struct CMLay {
+  static constexpr uint32_t SB = 0;                // [S_lo; S_hi]: fp32 K-major, 64 rows x 4 atoms (8 KB each)
+  static constexpr uint32_t TB = 32768;            // kTBufs buffers of T_j: 4 atoms of 128 rows x 128 B (16 KB)
+  static constexpr uint32_t TBUF = 65536;
+  static constexpr uint32_t BARS = TB + kTBufs * TBUF;
+  static constexpr uint32_t TOTAL = BARS + 64;
+  static constexpr uint32_t ALLOC = TOTAL + 1024;
+  // TMEM: two accumulators of 64 columns (0-31: rows of S_lo, 32-63: rows of S_hi; K steps 0-7
+  // and 8-15) and two T_lo buffers
+  static constexpr uint32_t cD = 0, cTL = 128;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(ALLOC <= 232448, "shared memory");
+  static_assert(kComposeCluster == 4, "one box of 32 fp32 columns per CTA of the cluster");
+};
+
+__global__ void __cluster_dims__(kComposeCluster, 1, 1) __launch_bounds__(kMapThreads, 1)
+    compose_tc_map_kernel(const __grid_constant__ CUtensorMap map_t, const ComposeParams p, int t_rows_per_op) {
+  using L = CMLay;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BARS);  // MMAs of a step
+  uint64_t* bar_ld = bar + 1;                                  // [kTBufs] T_j landed in this CTA
+  uint64_t* bar_free = bar_ld + kTBufs;                        // [kTBufs] buffer released by all four CTAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_free + kTBufs);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, hf = (warp >> 2) & 1;
+  const int h = blockIdx.y, row0 = blockIdx.x * CTR;
+  const int rank = (int)cluster_ctarank();  // = blockIdx.x: the quarter of T_j this CTA fetches
+  const int m = 32 * quad + lane;           // TMEM lane = d_k index of T's row / of the output column
+  const size_t hoff = (size_t)h * CTD * CTD;
+  constexpr int kCtl = CTNT / 32;           // the control warp
+  constexpr int kLoader = CTNT;             // its lane 0 owns the copies
+  const bool ctl = warp == kCtl;
+  constexpr uint32_t kTBytes = L::TBUF;     // bytes of T_j landing in each CTA per step
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == kLoader) {
+    mbar_init(bar, 1);
+    for (int b = 0; b < kTBufs; ++b) {
+      mbar_init(&bar_ld[b], 1);
+      mbar_init(&bar_free[b], kComposeCluster);
+    }
+    mbar_fence_init();
+    tma_prefetch_desc(&map_t);
+    for (int b = 0; b < kTBufs && b < p.K; ++b) mbar_arrive_expect_tx(&bar_ld[b], kTBytes);
+  }
+  // S_0 = S_in (or 0) -> rows 0-31 (lo) and 32-63 (hi) of the S tile: thread -> row tid / 8, 16 columns
+  if (!ctl) {
+    const int r = tid >> 3, k0 = (tid & 7) * 16;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p.S_in) v = *reinterpret_cast<const float4*>(p.S_in + hoff + (size_t)(row0 + r) * CTD + k0 + 4 * q);
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      float hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = tf32r(x[e]);
+        lo[e] = x[e] - hi[e];
+      }
+      *reinterpret_cast<float4*>(sm + L::SB + kf32(r, k0 + 4 * q, 64)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<float4*>(sm + L::SB + kf32(32 + r, k0 + 4 * q, 64)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every CTA's barriers are initialised before any copy or arrival reaches them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+  int timed_out = 0;  // this thread saw a bounded wait give up
+  // this CTA's copies of step s into buffer s % 3 (thread kLoader): its quarter of T_s to all
+  // four CTAs (expect_tx already posted for that phase), and its S_local_s rows into L2
+  auto issue_loads = [&](int s) {
+    const int b = s % kTBufs;
+    tma_load_2d_multicast(sm + L::TB + b * L::TBUF + rank * 16384, &map_t, &bar_ld[b], 64 * rank,
+                          s * t_rows_per_op + h * CTD, (uint16_t)((1u << kComposeCluster) - 1));
+    bulk_prefetch_l2(p.Slocal[s] + hoff + (size_t)row0 * CTD, CTR * 512);
+  };
+  auto ld_parity = [](int s) { return (uint32_t)((s / kTBufs) & 1); };
+  auto wait_ld = [&](int s) {
+    if (!mbar_wait(&bar_ld[s % kTBufs], ld_parity(s), p.wait_ns)) timed_out = 1;
+  };
+  // row m of T_s, columns [64 hf, 64 hf + 64), from the swizzled tile -> T - T_hi into T_lo buffer
+  // s & 1 (the 16-byte chunks of a row are XOR-swizzled by its index: a warp's rows hit distinct banks)
+  auto store_Tlo = [&](int s) {
+    const unsigned char* tile = sm + L::TB + (s % kTBufs) * L::TBUF + (uint32_t)m * 128u;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int a = 2 * hf + c;  // atom = 32 columns
+      float w[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 t = *reinterpret_cast<const float4*>(tile + a * 16384 + (((uint32_t)q ^ (m & 7u)) << 4));
+        const float x[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[4 * q + e] = x[e] - __uint_as_float(__float_as_uint(x[e]) & 0xffffe000u);
+      }
+      tmem_st32(tmem + lane_base + L::cTL + 128 * (s & 1) + 32 * a, w);
+    }
+  };
+  const uint64_t dS = sdesc_sw128(smem_u32(sm + L::SB), 16, 1024);          // [S_lo; S_hi], N = 64
+  const uint64_t dShi = sdesc_sw128(smem_u32(sm + L::SB + 4096), 16, 1024);  // S_hi rows, N = 32
+  const uint64_t dT = sdesc_sw128(smem_u32(sm + L::TB), 16, 1024);           // T_j, 128 rows, K-major
+  // step s's 32 MMAs, one issuing thread of the control warp, in K order; each T_lo S_hi term
+  // follows the T_hi [S_lo | S_hi] term of its K step, the first of which initialises its accumulator
+  auto issue = [&](int s) {
+    tc_fence_after();
+    constexpr uint32_t id64 = idesc_tf32(128, 64);
+    constexpr uint32_t id32 = idesc_tf32(128, CTR);
+    const uint64_t dTb = dadd_bytes(dT, (uint32_t)(s % kTBufs) * L::TBUF);
+    const uint32_t tl = tmem + L::cTL + 128 * (s & 1);
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;  // K step in the T tile (128-row atoms)
+      const uint32_t kb = (kk >> 2) * 8192 + (kk & 3) * 32;   // K step in the S tile (64-row atoms)
+      const uint32_t dc = tmem + L::cD + 64 * (kk >> 3);
+      if (elect_one()) {
+        mma_tf32(dc, dadd_bytes(dTb, ka), dadd_bytes(dS, kb), id64, (kk & 7) > 0);
+        mma_tf32_ts(dc + 32, tl + 8 * kk, dadd_bytes(dShi, kb), id32, true);
+      }
+    }
+    if (elect_one()) mma_commit(bar);
+    __syncwarp();
+  };
+
+  // thread kLoader's record: last step whose copies it issued, last step it released a buffer for
+  int issued = (p.K < kTBufs ? p.K : kTBufs) - 1, released = issued;
+  int mma_step = 0;  // last step whose MMAs were issued
+  if (ctl) {
+    if (tid == kLoader)
+      for (int s = 0; s <= issued; ++s) issue_loads(s);
+    __syncwarp();
+  } else {
+    wait_ld(0);
+    store_Tlo(0);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (ctl) issue(0);
+
+  if (ctl) {
+    // control warp: release and refill buffers, issue each step's MMAs once the compute warps
+    // have written its S tile and T_lo
+    for (int j = 0; j + 1 < p.K; ++j) {
+      if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) timed_out = 1;
+      tc_fence_after();
+      // T_j's readers are done (these MMAs; T_lo of step j was taken a step ago); once step j's
+      // copies are seen complete, post step j + 3's byte count and release the buffer everywhere
+      if (tid == kLoader && j + kTBufs < p.K && !timed_out &&
+          !mbar_wait(&bar_ld[j % kTBufs], ld_parity(j), p.wait_ns))
+        timed_out = 1;
+      if (tid == kLoader && j + kTBufs < p.K && !timed_out) {
+        mbar_arrive_expect_tx(&bar_ld[j % kTBufs], kTBytes);
+#pragma unroll
+        for (int c = 0; c < kComposeCluster; ++c) mbar_arrive_remote_relaxed(&bar_free[j % kTBufs], (uint32_t)c);
+        released = j + kTBufs;
+        if (mbar_wait_cluster(&bar_free[j % kTBufs], ld_parity(j), p.wait_ns)) {
+          issue_loads(j + kTBufs);
+          issued = j + kTBufs;
+        } else {
+          timed_out = 1;
+        }
+      }
+      __syncwarp();
+      if (__syncthreads_or(timed_out)) break;
+      issue(j + 1);
+      mma_step = j + 1;
+    }
+  } else {
+    for (int j = 0; j < p.K; ++j) {
+      // S_local_j[row0 + 16 hf + i][m] (consecutive m in a warp: coalesced), used by the epilogue
+      float sl[16];
+      {
+        const float* src = p.Slocal[j] + hoff + (size_t)(row0 + 16 * hf) * CTD + m;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sl[i] = __ldg(src + (size_t)i * CTD);
+      }
+      // while step j's MMAs run: T_lo of step j + 1 into the other TMEM buffer (step j - 1's MMAs,
+      // the last readers of that buffer, completed before the previous barrier)
+      if (j + 1 < p.K) {
+        wait_ld(j + 1);
+        store_Tlo(j + 1);
+      }
+      // step j's MMAs done: S_j = D + S_local_j
+      if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) timed_out = 1;
+      tc_fence_after();
+      float d[16], x[16], y[16];
+      tmem_ld16(tmem + lane_base + L::cD + 16 * hf, d);
+      tmem_ld16(tmem + lane_base + L::cD + 32 + 16 * hf, x);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) d[i] += x[i];
+      tmem_ld16(tmem + lane_base + L::cD + 64 + 16 * hf, x);
+      tmem_ld16(tmem + lane_base + L::cD + 96 + 16 * hf, y);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) d[i] += (x[i] + y[i]) + sl[i];
+      if (j + 1 == p.K) {
+        float* dst = p.S_out + hoff + (size_t)(row0 + 16 * hf) * CTD + m;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[(size_t)i * CTD] = d[i];
+        break;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float hi = tf32r(d[i]);
+        *reinterpret_cast<float*>(sm + L::SB + kf32(16 * hf + i, m, 64)) = d[i] - hi;
+        *reinterpret_cast<float*>(sm + L::SB + kf32(32 + 16 * hf + i, m, 64)) = hi;
+      }
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      // a wait that gave up in any thread stops the loop in every thread (the OR is taken by the barrier)
+      if (__syncthreads_or(timed_out)) break;
+    }
+  }
+
+  tc_fence_before();
+  if (__syncthreads_or(timed_out)) {
+    // A wait gave up.  Complete a step this CTA released but has not issued (its partners issue
+    // theirs when they see the same four releases), let the copies into this CTA land and the
+    // MMAs finish (each wait bounded at the default limit), then report.
+    if (tid == kLoader) {
+      if (released > issued) {
+        const int s = released;
+        if (mbar_wait_cluster(&bar_free[s % kTBufs], ld_parity(s - kTBufs), kWaitNs)) {
+          issue_loads(s);
+          issued = s;
+        }
+      }
+      // the latest phase of each buffer (its earlier phases completed before it was reissued)
+      for (int s = issued >= kTBufs - 1 ? issued - (kTBufs - 1) : 0; s <= issued; ++s)
+        mbar_wait(&bar_ld[s % kTBufs], ld_parity(s), kWaitNs);
+    }
+    if (tid == kLoader) {
+      mbar_wait(bar, (uint32_t)(mma_step & 1), kWaitNs);
+      atomicExch(p.status, GDN_ERR_TIMEOUT);
+    }
+    __syncthreads();
+  }
+  // no CTA leaves while a partner may still write into it or arrive on its barriers
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
 }  // namespace
 
 bool compose_tc_supported(const ComposeParams& p) { return p.d_k == CTD && p.d_v == CTD && p.K >= 1; }
 
 cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t stream) {
+  // One 2D view covers every T_j when they sit at one non-negative stride that is a whole number
+  // of 512-byte rows (one array of operators); otherwise each step's rows are copied one by one.
+  const char* t0 = reinterpret_cast<const char*>(p.T[0]);
+  const ptrdiff_t stride = p.K > 1 ? reinterpret_cast<const char*>(p.T[1]) - t0 : 0;
+  bool uniform = stride >= 0 && stride % 512 == 0;
+  for (int j = 2; uniform && j < p.K; ++j) uniform = reinterpret_cast<const char*>(p.T[j]) == t0 + j * stride;
+  const uint64_t rows_per_op = (uint64_t)stride / 512;
+  const uint64_t rows = (uint64_t)(p.K - 1) * rows_per_op + (uint64_t)p.h * CTD;
+  CUtensorMap map;
+  if (uniform && rows < (1ull << 31) && make_map(&map, t0, rows, 2 * CTD, CTD)) {
+    cudaError_t e = cudaFuncSetAttribute(compose_tc_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)CMLay::ALLOC);
+    if (e != cudaSuccess) return e;
+    compose_tc_map_kernel<<<dim3(CTD / CTR, p.h), kMapThreads, CMLay::ALLOC, stream>>>(map, p, (int)rows_per_op);
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)CTLay::ALLOC);
   if (e != cudaSuccess) return e;

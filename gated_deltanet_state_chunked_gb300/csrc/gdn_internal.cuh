@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +66,11 @@ cudaError_t launch_compose_simt(const ComposeParams& p, cudaStream_t stream);
 // Tensor-core composition (split tf32, fp32 accuracy) for d_k = d_v = 128 and K >= 1.
 bool compose_tc_supported(const ComposeParams& p);
 cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t stream);
+
+// Tensor map of a 2D bf16 view [rows][cols] (cols contiguous) with boxes of 64 columns x
+// box_rows rows, 128-byte swizzle (the tile layout the tensor-core operands use); false if the
+// driver's encoder is unavailable or rejects the view.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 // Sticky status word of the current device (device pointer).
 int* device_status_word();

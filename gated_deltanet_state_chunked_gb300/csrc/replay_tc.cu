@@ -987,6 +987,8 @@ __global__ void __launch_bounds__(NT, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1000,18 +1002,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 view [rows][cols] (cols contiguous), 64 x 64 boxes, 128-byte swizzle, zero fill out of range.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+// 2D bf16 view [rows][cols] (cols contiguous), boxes of 64 columns x box_rows rows, 128-byte
+// swizzle, zero fill out of range.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int R>
 cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ScanParams& sp,
@@ -1086,9 +1091,9 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   if (workspace_bytes < replay_tc_workspace_bytes(p.n_seqs, p.total_tokens, p.h_v)) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv;
   const void* qsrc = p.write_O ? p.q : p.k;  // q unused without outputs: any valid tile source
-  if (!make_map(&mq, qsrc, p.total_tokens, (uint64_t)p.h_k * DK) ||
-      !make_map(&mk, p.k, p.total_tokens, (uint64_t)p.h_k * DK) ||
-      !make_map(&mv, p.v, p.total_tokens, (uint64_t)p.h_v * DV))
+  if (!make_map(&mq, qsrc, p.total_tokens, (uint64_t)p.h_k * DK, 64) ||
+      !make_map(&mk, p.k, p.total_tokens, (uint64_t)p.h_k * DK, 64) ||
+      !make_map(&mv, p.v, p.total_tokens, (uint64_t)p.h_v * DV, 64))
     return cudaErrorInvalidValue;
   unsigned char* rec = static_cast<unsigned char*>(workspace);
   int32_t* order = nullptr;

@@ -144,13 +144,30 @@ def test_chunk_operator_matches_oracle(dtype):
     assert rel_err(host(Sl), Sl_ref) <= TOL_F32
 
 
-def test_compose_matches_oracle_closed_form():
+def _ops_on_device(T, layout):
+    """The K operators as a list of device tensors.  "one_array": views of one [K, ...] tensor
+    (one stride between operators: the tensor-map kernel); "scattered": views of one tensor at
+    permuted positions (no common stride: the kernel that copies rows one by one)."""
+    K = T.shape[0]
+    if layout == "one_array":
+        Td = torch.from_numpy(np.ascontiguousarray(T)).cuda()
+        return [Td[j] for j in range(K)]
+    # reversed slots, the first one step further out: a negative stride for K = 2, none for K > 2
+    perm = [K - 1 - j + (1 if j == 0 else 0) for j in range(K)]
+    big = torch.zeros((K + 2,) + T.shape[1:], dtype=torch.float32, device="cuda")
+    for j in range(K):
+        big[perm[j]] = torch.from_numpy(T[j]).cuda()
+    return [big[perm[j]] for j in range(K)]
+
+
+@pytest.mark.parametrize("layout", ["one_array", "scattered"])
+def test_compose_matches_oracle_closed_form(layout):
     rng = np.random.Generator(np.random.PCG64(14))
     K, h, dk, dv = 6, 4, 128, 128
     T = (rng.standard_normal((K, h, dk, dk)) / np.sqrt(dk)).astype(np.float32)
     Sl = rng.standard_normal((K, h, dv, dk)).astype(np.float32)
     S_in = rng.standard_normal((h, dv, dk)).astype(np.float32)
-    Td = [torch.from_numpy(T[j]).cuda() for j in range(K)]
+    Td = _ops_on_device(T, layout)
     Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
     out = api.gdn_compose(Td, Sd, torch.from_numpy(S_in).cuda())
     out0 = api.gdn_compose(Td, Sd, None)
@@ -159,16 +176,17 @@ def test_compose_matches_oracle_closed_form():
     assert rel_err(host(out0), oracle.compose(T, Sl, None)) <= TOL_F32
 
 
-@pytest.mark.parametrize("K", [0, 1, 2])
-def test_compose_edge_counts(K):
-    """K = 0 copies S_in (or writes zeros); K = 1 and 2 exercise the first and last step of the
-    tensor-core composition (128-dim heads) on their own."""
+@pytest.mark.parametrize("layout", ["one_array", "scattered"])
+@pytest.mark.parametrize("K", [0, 1, 2, 3])
+def test_compose_edge_counts(K, layout):
+    """K = 0 copies S_in (or writes zeros); K = 1, 2 and 3 exercise the first and last steps of
+    the tensor-core composition (128-dim heads) and both copy buffers on their own."""
     rng = np.random.Generator(np.random.PCG64(40 + K))
     h, d = 3, 128
     T = (rng.standard_normal((K, h, d, d)) / np.sqrt(d)).astype(np.float32)
     Sl = rng.standard_normal((K, h, d, d)).astype(np.float32)
     S_in = rng.standard_normal((h, d, d)).astype(np.float32)
-    Td = [torch.from_numpy(T[j]).cuda() for j in range(K)]
+    Td = _ops_on_device(T, layout) if K else []
     Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
     out = api.gdn_compose(Td, Sd, torch.from_numpy(S_in).cuda())
     torch.cuda.synchronize()
@@ -198,8 +216,9 @@ def test_composed_chunks_equal_sequential_replay():
     assert rel_err(host(S[0]), S_ref[0]) <= TOL_F32
 
 
+@pytest.mark.parametrize("layout", ["one_array", "scattered"])
 @pytest.mark.parametrize("K", [1, 5])
-def test_compose_wait_that_runs_out_reports_timeout_then_recovers(K):
+def test_compose_wait_that_runs_out_reports_timeout_then_recovers(K, layout):
     """The bounded-wait path without a fault: with a wait limit of zero the first wait on the
     MMAs gives up, the kernel lets its issued MMAs finish and reports GDN_ERR_TIMEOUT; the
     context stays usable and the next call (default limit) is correct."""
@@ -207,7 +226,7 @@ def test_compose_wait_that_runs_out_reports_timeout_then_recovers(K):
     h, d = 4, 128
     T = (rng.standard_normal((K, h, d, d)) / np.sqrt(d)).astype(np.float32)
     Sl = rng.standard_normal((K, h, d, d)).astype(np.float32)
-    Td = [torch.from_numpy(T[j]).cuda() for j in range(K)]
+    Td = _ops_on_device(T, layout)
     Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
     api.gdn_set_wait_limit_ns(0)
     api.gdn_compose(Td, Sd, None)
