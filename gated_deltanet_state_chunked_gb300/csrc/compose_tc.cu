@@ -259,22 +259,25 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
 // row is a row of one 2D view, so a step's T_j arrives by tensor copies (128 rows x 128 B boxes,
 // 128-byte swizzle), already in the layout of a K-major tensor-core operand.  The four CTAs of
 // a head form a cluster: each fetches one quarter (32 columns) of T_j and multicasts it to all
-// four, so T_j leaves L2 once per head instead of four times.  Per step:
-//   T_hi [S_lo | S_hi]  one product of N = 64, A = the T_j tile itself in shared memory (the
-//                       tensor core reads fp32 as tf32, dropping the low 13 mantissa bits);
+// four, so T_j leaves L2 once per head instead of four times.  Each thread reads its row of T_j
+// (its half of the columns) from the tile once; both operands of the step go to TMEM from there:
+//   T_hi [S_lo | S_hi]  one product of N = 64, A = T itself in TMEM (the tensor core reads fp32
+//                       as tf32, dropping the low 13 mantissa bits);
 //   T_lo S_hi           N = 32, A = T - T_hi in TMEM (exact in fp32), accumulated into the S_hi
 //                       half of the same accumulator;
 // with K split over two accumulators (added by the epilogue in fp32).  T_lo of step j + 1 is
-// written into the other of two TMEM buffers while step j's MMAs run, so the serial chain per
-// step is the MMAs and the epilogue (D + S_local -> the split S tile).  T_j sits in one of three
-// shared-memory buffers, so copies run about two steps ahead; S_local_j is read into registers
-// at the top of step j, from L2, where it was prefetched when step j's copies were issued.
+// written into the other of two TMEM buffers while step j's MMAs run, and T itself into its one
+// buffer right after them, so the serial chain per step is the MMAs and the epilogue (D +
+// S_local -> the split S tile, T_{j+1} -> TMEM).  The tensor core reads only the S tile from
+// shared memory.  T_j sits in one of three shared-memory buffers, refilled as soon as the threads
+// have read it, so copies run about three steps ahead; S_local_j is read into registers at the
+// top of step j, from L2, where it was prefetched when step j's copies were issued.
 //
-// Warps 0-7 prepare T_lo and run the epilogue; warp 8 issues the MMAs and owns the copies.
-// Copy protocol: after step j's MMAs complete, the CTA posts its
-// own expect_tx for step j + 3 and releases buffer j % 3 by arriving on the "free" barrier of
-// that buffer in all four CTAs; it issues its quarter of step j + 3 once its own free barrier has
-// all four arrivals.  Every CTA sees the same four arrivals, so a step is issued by all four or
+// Warps 0-7 read T, prepare T_lo and run the epilogue; warp 8 issues the MMAs and owns the
+// copies.  Copy protocol: once every thread has read T_s (the barrier before step s - 1's MMAs),
+// the CTA posts its own expect_tx for step s + 3 and releases buffer s % 3 by arriving on the
+// "free" barrier of that buffer in all four CTAs; it issues its quarter of step s + 3 once its
+// own free barrier has all four arrivals.  Every CTA sees the same four arrivals, so a step is issued by all four or
 // by none, and a CTA that stops early (a bounded wait gave up) completes any step it released
 // before it leaves; a final cluster barrier keeps every CTA alive until its partners are done.
 // ---------------------------------------------------------------------------------------------
@@ -290,8 +293,8 @@ struct CMLay {
   static constexpr uint32_t TOTAL = BARS + 64;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
   // TMEM: two accumulators of 64 columns (0-31: rows of S_lo, 32-63: rows of S_hi; K steps 0-7
-  // and 8-15) and two T_lo buffers
-  static constexpr uint32_t cD = 0, cTL = 128;
+  // and 8-15), T and two T_lo buffers
+  static constexpr uint32_t cD = 0, cTH = 128, cTL = 256;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(ALLOC <= 232448, "shared memory");
   static_assert(kComposeCluster == 4, "one box of 32 fp32 columns per CTA of the cluster");
@@ -368,42 +371,52 @@ __global__ void __cluster_dims__(kComposeCluster, 1, 1) __launch_bounds__(kMapTh
   auto wait_ld = [&](int s) {
     if (!mbar_wait(&bar_ld[s % kTBufs], ld_parity(s), p.wait_ns)) timed_out = 1;
   };
-  // row m of T_s, columns [64 hf, 64 hf + 64), from the swizzled tile -> T - T_hi into T_lo buffer
-  // s & 1 (the 16-byte chunks of a row are XOR-swizzled by its index: a warp's rows hit distinct banks)
-  auto store_Tlo = [&](int s) {
+  // row m of T_s, columns [64 hf, 64 hf + 64), from the swizzled tile into tr (the 16-byte
+  // chunks of a row are XOR-swizzled by its index: a warp's rows hit distinct banks), and
+  // T - T_hi into T_lo buffer s & 1
+  float tr[64];
+  auto load_T = [&](int s) {
     const unsigned char* tile = sm + L::TB + (s % kTBufs) * L::TBUF + (uint32_t)m * 128u;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int a = 2 * hf + c;  // atom = 32 columns
-      float w[32];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float4 t = *reinterpret_cast<const float4*>(tile + a * 16384 + (((uint32_t)q ^ (m & 7u)) << 4));
-        const float x[4] = {t.x, t.y, t.z, t.w};
+        tr[32 * c + 4 * q] = t.x;
+        tr[32 * c + 4 * q + 1] = t.y;
+        tr[32 * c + 4 * q + 2] = t.z;
+        tr[32 * c + 4 * q + 3] = t.w;
+      }
+      float w[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) w[4 * q + e] = x[e] - __uint_as_float(__float_as_uint(x[e]) & 0xffffe000u);
+      for (int e = 0; e < 32; ++e) {
+        const float x = tr[32 * c + e];
+        w[e] = x - __uint_as_float(__float_as_uint(x) & 0xffffe000u);
       }
       tmem_st32(tmem + lane_base + L::cTL + 128 * (s & 1) + 32 * a, w);
     }
   };
+  // T itself (the row held in tr) into the T buffer, once the MMAs reading the previous T are done
+  auto store_T = [&]() {
+    tmem_st32(tmem + lane_base + L::cTH + 64 * hf, *reinterpret_cast<const float(*)[32]>(tr));
+    tmem_st32(tmem + lane_base + L::cTH + 64 * hf + 32, *reinterpret_cast<const float(*)[32]>(tr + 32));
+  };
   const uint64_t dS = sdesc_sw128(smem_u32(sm + L::SB), 16, 1024);          // [S_lo; S_hi], N = 64
   const uint64_t dShi = sdesc_sw128(smem_u32(sm + L::SB + 4096), 16, 1024);  // S_hi rows, N = 32
-  const uint64_t dT = sdesc_sw128(smem_u32(sm + L::TB), 16, 1024);           // T_j, 128 rows, K-major
   // step s's 32 MMAs, one issuing thread of the control warp, in K order; each T_lo S_hi term
   // follows the T_hi [S_lo | S_hi] term of its K step, the first of which initialises its accumulator
   auto issue = [&](int s) {
     tc_fence_after();
     constexpr uint32_t id64 = idesc_tf32(128, 64);
     constexpr uint32_t id32 = idesc_tf32(128, CTR);
-    const uint64_t dTb = dadd_bytes(dT, (uint32_t)(s % kTBufs) * L::TBUF);
     const uint32_t tl = tmem + L::cTL + 128 * (s & 1);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;  // K step in the T tile (128-row atoms)
-      const uint32_t kb = (kk >> 2) * 8192 + (kk & 3) * 32;   // K step in the S tile (64-row atoms)
+      const uint32_t kb = (kk >> 2) * 8192 + (kk & 3) * 32;  // K step in the S tile (64-row atoms)
       const uint32_t dc = tmem + L::cD + 64 * (kk >> 3);
       if (elect_one()) {
-        mma_tf32(dc, dadd_bytes(dTb, ka), dadd_bytes(dS, kb), id64, (kk & 7) > 0);
+        mma_tf32_ts(dc, tmem + L::cTH + 8 * kk, dadd_bytes(dS, kb), id64, (kk & 7) > 0);
         mma_tf32_ts(dc + 32, tl + 8 * kk, dadd_bytes(dShi, kb), id32, true);
       }
     }
@@ -414,46 +427,49 @@ __global__ void __cluster_dims__(kComposeCluster, 1, 1) __launch_bounds__(kMapTh
   // thread kLoader's record: last step whose copies it issued, last step it released a buffer for
   int issued = (p.K < kTBufs ? p.K : kTBufs) - 1, released = issued;
   int mma_step = 0;  // last step whose MMAs were issued
+  // thread kLoader, once every thread has read T_{s - 3}: release its buffer for step s (after
+  // seeing step s - 3's copies complete) and, once all four CTAs have, issue step s's copies
+  auto refill = [&](int s) {
+    const int b = s % kTBufs;
+    if (timed_out || !mbar_wait(&bar_ld[b], ld_parity(s - kTBufs), p.wait_ns)) {
+      timed_out = 1;
+      return;
+    }
+    mbar_arrive_expect_tx(&bar_ld[b], kTBytes);
+#pragma unroll
+    for (int c = 0; c < kComposeCluster; ++c) mbar_arrive_remote_relaxed(&bar_free[b], (uint32_t)c);
+    released = s;
+    if (mbar_wait_cluster(&bar_free[b], ld_parity(s - kTBufs), p.wait_ns)) {
+      issue_loads(s);
+      issued = s;
+    } else {
+      timed_out = 1;  // the loop stops at a later barrier (the copy waits give up)
+    }
+  };
   if (ctl) {
     if (tid == kLoader)
       for (int s = 0; s <= issued; ++s) issue_loads(s);
     __syncwarp();
   } else {
     wait_ld(0);
-    store_Tlo(0);
+    load_T(0);
+    store_T();
     tmem_st_wait();
   }
   tc_fence_before();
   __syncthreads();
-  if (ctl) issue(0);
-
   if (ctl) {
-    // control warp: release and refill buffers, issue each step's MMAs once the compute warps
-    // have written its S tile and T_lo
+    issue(0);
+    if (tid == kLoader && kTBufs < p.K) refill(kTBufs);  // T_0 has been read
+    __syncwarp();
+    // control warp: issue each step's MMAs once the compute warps have written its S tile, T and
+    // T_lo; then refill the buffer of the T they read before that barrier
     for (int j = 0; j + 1 < p.K; ++j) {
-      if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) timed_out = 1;
-      tc_fence_after();
-      // T_j's readers are done (these MMAs; T_lo of step j was taken a step ago); once step j's
-      // copies are seen complete, post step j + 3's byte count and release the buffer everywhere
-      if (tid == kLoader && j + kTBufs < p.K && !timed_out &&
-          !mbar_wait(&bar_ld[j % kTBufs], ld_parity(j), p.wait_ns))
-        timed_out = 1;
-      if (tid == kLoader && j + kTBufs < p.K && !timed_out) {
-        mbar_arrive_expect_tx(&bar_ld[j % kTBufs], kTBytes);
-#pragma unroll
-        for (int c = 0; c < kComposeCluster; ++c) mbar_arrive_remote_relaxed(&bar_free[j % kTBufs], (uint32_t)c);
-        released = j + kTBufs;
-        if (mbar_wait_cluster(&bar_free[j % kTBufs], ld_parity(j), p.wait_ns)) {
-          issue_loads(j + kTBufs);
-          issued = j + kTBufs;
-        } else {
-          timed_out = 1;
-        }
-      }
-      __syncwarp();
       if (__syncthreads_or(timed_out)) break;
       issue(j + 1);
       mma_step = j + 1;
+      if (tid == kLoader && j + 1 + kTBufs < p.K) refill(j + 1 + kTBufs);
+      __syncwarp();
     }
   } else {
     for (int j = 0; j < p.K; ++j) {
@@ -464,11 +480,11 @@ __global__ void __cluster_dims__(kComposeCluster, 1, 1) __launch_bounds__(kMapTh
 #pragma unroll
         for (int i = 0; i < 16; ++i) sl[i] = __ldg(src + (size_t)i * CTD);
       }
-      // while step j's MMAs run: T_lo of step j + 1 into the other TMEM buffer (step j - 1's MMAs,
-      // the last readers of that buffer, completed before the previous barrier)
+      // while step j's MMAs run: T_{j+1} into registers and its T_lo into the other TMEM buffer
+      // (step j - 1's MMAs, the last readers of that buffer, completed before the previous barrier)
       if (j + 1 < p.K) {
         wait_ld(j + 1);
-        store_Tlo(j + 1);
+        load_T(j + 1);
       }
       // step j's MMAs done: S_j = D + S_local_j
       if (!mbar_wait(bar, (uint32_t)(j & 1), p.wait_ns)) timed_out = 1;
@@ -490,6 +506,7 @@ __global__ void __cluster_dims__(kComposeCluster, 1, 1) __launch_bounds__(kMapTh
         for (int i = 0; i < 16; ++i) dst[(size_t)i * CTD] = d[i];
         break;
       }
+      store_T();  // step j's MMAs, the readers of the T buffer, are done
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float hi = tf32r(d[i]);

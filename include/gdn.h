@@ -176,6 +176,13 @@ int gdn_chunk_operator(const gdn_dims* dims, const void* k, const float* g, cons
  *               Slocal[j] fp32 [h_v][d_v][d_k]
  *   S_in        fp32 [h_v][d_v][d_k] or NULL (empty entering state)
  *   S_out       fp32 [h_v][d_v][d_k]; must not alias any input
+ * With d_k = d_v = 128 the tensor cores do the products (T and S each split
+ * into a tf32 part and an exact fp32 remainder; three products per step,
+ * fp32 accuracy).  When the T[j] sit at one non-negative stride that is a
+ * multiple of 512 bytes (e.g. the K slices of one [K][h_v][d_k][d_k] array)
+ * each step's T arrives by tensor copies shared across the four CTAs of a
+ * head; other pointer arrays take a slower path that copies T row by row.
+ * Both give the same results up to fp32 rounding order.
  */
 int gdn_compose(const gdn_dims* dims, int32_t K, const float* const* T, const float* const* Slocal,
                 const float* S_in, float* S_out, void* stream);

@@ -200,6 +200,23 @@ def test_compose_edge_counts(K, layout):
         assert rel_err(host(out0), oracle.compose(T, Sl, None)) <= TOL_F32
 
 
+@pytest.mark.parametrize("layout", ["one_array", "scattered"])
+def test_compose_long_chain(layout):
+    """K = 40: every copy buffer and barrier phase of the tensor-core composition wraps many
+    times; the error stays within the fp32 tolerance over the whole chain."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    K, h, d = 40, 2, 128
+    T = (rng.standard_normal((K, h, d, d)) / np.sqrt(d)).astype(np.float32)
+    Sl = rng.standard_normal((K, h, d, d)).astype(np.float32)
+    S_in = rng.standard_normal((h, d, d)).astype(np.float32)
+    Td = _ops_on_device(T, layout)
+    Sd = [torch.from_numpy(Sl[j]).cuda() for j in range(K)]
+    out = api.gdn_compose(Td, Sd, torch.from_numpy(S_in).cuda())
+    torch.cuda.synchronize()
+    api.gdn_get_status()
+    assert rel_err(host(out), oracle.compose(T, Sl, S_in)) <= TOL_F32
+
+
 def test_composed_chunks_equal_sequential_replay():
     """LinearKV composition passage: composing isolated-chunk operators is exact, so
     compose(chunk operators) on the GPU equals the GPU's own sequential replay."""
