@@ -34,6 +34,13 @@ struct SimtParams {
   unsigned char* rec;  // optional per-(chunk, v-head) records of the chunk-shared quantities (scratch)
 };
 
+// fp32 record of the chunk-shared quantities of one (chunk, v-head), written by the fp32 path's
+// prep kernel: M = (I + A)^{-1} [64][64] (row t, column s), P [64][64] (only when outputs are
+// wanted), then per token t: gamma_t, exp(G_last - G_t), beta_t, rk_t (key norm factor), rq_t
+// (query norm factor times scale).  Offsets in floats.
+constexpr int REC_M = 0, REC_P = 4096, REC_GAM = 8192, REC_WEND = 8256, REC_BETA = 8320, REC_RK = 8384,
+              REC_RQ = 8448, REC_FLOATS = 8512;
+
 cudaError_t launch_replay_simt(const SimtParams& p, int bf16, cudaStream_t stream);
 // Scratch bytes of the two-kernel CUDA-core path (chunk-parallel prep, then the row-slice scan).
 size_t simt_records_bytes(int n_seqs, int total_tokens, int h_v);
@@ -71,6 +78,13 @@ cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t stream);
 // box_rows rows, 128-byte swizzle (the tile layout the tensor-core operands use); false if the
 // driver's encoder is unavailable or rejects the view.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// The same for a 2D fp32 view: boxes of 32 columns (128 bytes) x box_rows rows.
+bool make_map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// Tensor-core state-only scan of the fp32 path (d_k = d_v = 128, fp32 inputs, no outputs), over
+// the records already written into p.rec: the state (augmented or not) in 128-row slices.
+bool chunkop_tc_supported(const SimtParams& p, int bf16);
+cudaError_t launch_chunkop_tc(const SimtParams& p, cudaStream_t stream);
 
 // Sticky status word of the current device (device pointer).
 int* device_status_word();

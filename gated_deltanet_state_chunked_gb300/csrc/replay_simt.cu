@@ -93,11 +93,8 @@ __device__ __forceinline__ void st_out(float* p, size_t i, float x) { p[i] = x; 
 __device__ __forceinline__ void st_out(__nv_bfloat16* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 
 // ---------------------------------------------------------------------------------------------
-// Two-pass mode: the chunk-shared quantities, once per (chunk, v-head).  Record (fp32):
-//   M = (I + A)^{-1} [64][64], P [64][64] (zero without outputs), gamma_t, exp(G_last - G_t),
-//   beta_t, rk_t (key norm factor), rq_t (query norm factor times scale).
-constexpr int REC_M = 0, REC_P = 4096, REC_GAM = 8192, REC_WEND = 8256, REC_BETA = 8320, REC_RK = 8384,
-              REC_RQ = 8448, REC_FLOATS = 8512;
+// Two-pass mode: the chunk-shared quantities, once per (chunk, v-head), in the fp32 record
+// layout of gdn_internal.cuh (REC_*).
 
 struct PrepSmem {
   float K[C * KST];
@@ -181,38 +178,31 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
     sm.G[lane + 32] = b;
   }
   __syncthreads();
-  {  // Gram matrices: A (strictly lower, gated, beta-weighted) into shared memory, P into the record
-    const int ti = (tid / 16) * 4, si = (tid % 16) * 4;
+  {  // Gram matrices on warp-level tensor cores (split tf32): A (strictly lower, gated,
+     // beta-weighted) into shared memory, P into the record (only when outputs are wanted: the
+     // scan reads it for nothing else).  Warp w -> rows 16 (w % 4) + [0, 16), columns 32 (w / 4) + [0, 32).
+    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), g = lane >> 2, q4 = lane & 3;
     float akk[4][4] = {}, aqk[4][4] = {};
-    for (int d = 0; d < DK; ++d) {
-      float a[4], b[4], c[4];
+    tcp::warp_mma_tf32x3<4>(akk, [&](int m, int kk) { return sm.K[m * KST + kk]; },
+                            [&](int kk, int nn) { return sm.K[nn * KST + kk]; }, m0, n0, 0, DK, C);
+    if (p.write_O)
+      tcp::warp_mma_tf32x3<4>(aqk, [&](int m, int kk) { return sm.Q[m * KST + kk]; },
+                              [&](int kk, int nn) { return sm.K[nn * KST + kk]; }, m0, n0, 0, DK, C);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = sm.K[(ti + i) * KST + d];
-        b[i] = sm.K[(si + i) * KST + d];
-        c[i] = p.write_O ? sm.Q[(ti + i) * KST + d] : 0.f;
-      }
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t = m0 + g + 8 * hh, s0 = n0 + 8 * j + 2 * q4;
+        float pv[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          akk[i][j] = fmaf(a[i], b[j], akk[i][j]);
-          aqk[i][j] = fmaf(c[i], b[j], aqk[i][j]);
+        for (int e = 0; e < 2; ++e) {
+          const int s = s0 + e;
+          const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
+          sm.A[t * tcp::MST + s] = (s < t && !p.scalar_decay) ? sm.beta[t] * decay * akk[j][2 * hh + e] : 0.f;
+          pv[e] = s <= t ? decay * aqk[j][2 * hh + e] : 0.f;
         }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = ti + i;
-      float pv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int s = si + j;
-        const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
-        sm.A[t * tcp::MST + s] = (s < t && !p.scalar_decay) ? sm.beta[t] * decay * akk[i][j] : 0.f;
-        pv[j] = s <= t ? decay * aqk[i][j] : 0.f;
+        if (p.write_O) *reinterpret_cast<float2*>(rec + REC_P + t * C + s0) = make_float2(pv[0], pv[1]);
       }
-      *reinterpret_cast<float4*>(rec + REC_P + t * C + si) = make_float4(pv[0], pv[1], pv[2], pv[3]);
-    }
   }
   __syncthreads();
   if (warp < 4) {
@@ -657,6 +647,8 @@ cudaError_t launch_replay_simt_two_pass(SimtParams p, int bf16, void* workspace,
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // state only, fp32, 128-dim heads: the tensor-core scan over the same records
+  if (chunkop_tc_supported(p, bf16)) return launch_chunkop_tc(p, stream);
   return launch_replay_simt(p, bf16, stream);
 }
 
