@@ -171,6 +171,10 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     if (tid == 0 && c + 1 < n_chunks) {
       issue_k(c + 1);
       k_issued = c + 1;
+      // and its M and factors into L2 (read by every thread at the top of that chunk)
+      const float* Rn = R_ + (size_t)p.h_v * REC_FLOATS;
+      bulk_prefetch_l2(Rn + REC_M, 4096 * 4);
+      bulk_prefetch_l2(Rn + REC_GAM, 256 * 4);
     }
     // this chunk's values (row r, tokens [32 hf, +32)) and M, factors: loads in flight while the
     // keys are transposed

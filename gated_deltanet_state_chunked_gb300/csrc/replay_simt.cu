@@ -31,6 +31,8 @@
 // beta = 0, g = 0: identity transitions whose outputs are not stored.
 #include <cuda_bf16.h>
 
+#include <cstddef>
+
 #include "gdn_internal.cuh"
 #include "tc_common.cuh"
 
@@ -98,12 +100,13 @@ __device__ __forceinline__ void st_out(__nv_bfloat16* p, size_t i, float x) { p[
 
 struct PrepSmem {
   float K[C * KST];
-  float Q[C * KST];
   float A[C * tcp::MST];
   float M[C * tcp::MST];
   float G[C], beta[C], rk[C], rq[C];
   int scratch[20];
+  float Q[C * KST];  // last: not allocated when no outputs are wanted
 };
+constexpr size_t kPrepSmemNoQ = offsetof(PrepSmem, Q);
 
 // One CTA per (global chunk, v-head): load and normalise the chunk's keys (and queries), gate
 // sums, the gated Gram matrices A and P, and M = (I + A)^{-1}; write the record.
@@ -130,12 +133,37 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
   const Tin* __restrict__ k = static_cast<const Tin*>(p.k);
   float* rec = reinterpret_cast<float*>(p.rec) + ((size_t)gc * p.h_v + h) * REC_FLOATS;
 
+  bool loaded = false;
+  if constexpr (sizeof(Tin) == 4) {
+    if (DK == kMaxHead) {  // fp32, 128-dim heads: every 16-byte load of the tile issued at once
+      const float* kf = reinterpret_cast<const float*>(k);
+      const float* qf = reinterpret_cast<const float*>(q);
+      float4 kv[8], qv[8];
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+        const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d4;
+        kv[j] = t < n ? *reinterpret_cast<const float4*>(kf + off) : z4;
+        qv[j] = (p.write_O && t < n) ? *reinterpret_cast<const float4*>(qf + off) : z4;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+        *reinterpret_cast<float4*>(sm.K + t * KST + d4) = kv[j];
+        if (p.write_O) *reinterpret_cast<float4*>(sm.Q + t * KST + d4) = qv[j];
+      }
+      loaded = true;
+    }
+  }
+  if (!loaded) {
 #pragma unroll 8
-  for (int i = tid; i < C * DK; i += NT) {
-    const int t = i / DK, d = i % DK;
-    const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d;
-    sm.K[t * KST + d] = t < n ? ld_in(k, off) : 0.f;
-    if (p.write_O) sm.Q[t * KST + d] = t < n ? ld_in(q, off) : 0.f;
+    for (int i = tid; i < C * DK; i += NT) {
+      const int t = i / DK, d = i % DK;
+      const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d;
+      sm.K[t * KST + d] = t < n ? ld_in(k, off) : 0.f;
+      if (p.write_O) sm.Q[t * KST + d] = t < n ? ld_in(q, off) : 0.f;
+    }
   }
   if (tid < C) {
     const bool in = tid < n;
@@ -632,7 +660,7 @@ cudaError_t launch_replay_simt_two_pass(SimtParams p, int bf16, void* workspace,
   const int chunks_ub = tcp::chunks_of(p.total_tokens) + (p.cu ? p.n_seqs : 0);
   if (p.total_tokens > 0) {
     const dim3 grid(chunks_ub, p.h_v);
-    const size_t smem = sizeof(PrepSmem);
+    const size_t smem = p.write_O ? sizeof(PrepSmem) : kPrepSmemNoQ;
     cudaError_t e;
     if (bf16) {
       e = cudaFuncSetAttribute(simt_chunk_prep_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
