@@ -156,6 +156,25 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     ++mph;
     tc_fence_after();
   };
+  // chunk c's M (and its lo part) into the M tile; this thread's one of the 256 factor floats
+  // (gamma, exp(G_C - G_t), beta, rk) is returned, for the factor table once its readers are done
+  auto load_rec = [&](int c) {
+    const float* Rc = p.rec + ((size_t)(first + c) * p.h_v + h) * REC_FLOATS;
+    float4 mv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mv[j] = *reinterpret_cast<const float4*>(Rc + REC_M + (tid + j * NT) * 4);
+    const float fac = Rc[REC_GAM + tid];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // M (row t, columns s4..s4+3) and its lo part
+      const int i4 = tid + j * NT, t = i4 >> 4, s4 = (i4 & 15) * 4;
+      const float4 m = mv[j];
+      *reinterpret_cast<float4*>(sm + L::MT + kf32(t, s4, 128)) = m;
+      *reinterpret_cast<float4*>(sm + L::MT + kf32(64 + t, s4, 128)) =
+          make_float4(tf32_lo(m.x), tf32_lo(m.y), tf32_lo(m.z), tf32_lo(m.w));
+    }
+    return fac;
+  };
+  float fac_next = n_chunks > 0 ? load_rec(0) : 0.f;
   const uint64_t dKTT = sdesc_sw128(smem_u32(sm + L::KTT), 16, 1024);
   const uint64_t dMT = sdesc_sw128(smem_u32(sm + L::MT), 16, 1024);
   constexpr uint32_t id128 = idesc_tf32(128, 128);
@@ -165,43 +184,36 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     const int t0 = t_begin + c * C, n = min(C, t_end - t0);
     const int b = c & 1;
     unsigned char* kt = sm + L::KT + b * L::KTBUF;
-    const float* R_ = p.rec + ((size_t)(first + c) * p.h_v + h) * REC_FLOATS;
     // the next chunk's raw keys into the other buffer (its last readers, chunk c - 1's D1 and
     // transposition, finished before that chunk's state update)
     if (tid == 0 && c + 1 < n_chunks) {
       issue_k(c + 1);
       k_issued = c + 1;
-      // and its M and factors into L2 (read by every thread at the top of that chunk)
-      const float* Rn = R_ + (size_t)p.h_v * REC_FLOATS;
+      // and its M and factors into L2 (read while this chunk's state update runs)
+      const float* Rn = p.rec + ((size_t)(first + c + 1) * p.h_v + h) * REC_FLOATS;
       bulk_prefetch_l2(Rn + REC_M, 4096 * 4);
       bulk_prefetch_l2(Rn + REC_GAM, 256 * 4);
     }
-    // this chunk's values (row r, tokens [32 hf, +32)) and M, factors: loads in flight while the
-    // keys are transposed
+    // this chunk's factors (loaded during the previous state update; their readers are done)
+    fGam[tid] = fac_next;
+    // this chunk's values (row r, tokens [32 hf, +32)): loads in flight while the keys are transposed
     float vv[32];
+    if (slice == 0) {
+      const float* vp = p.v + ((size_t)(t0 + 32 * hf) * p.h_v + h) * D + rg;
+      const size_t vs = (size_t)p.h_v * D;
+      const int nv = n - 32 * hf;  // tokens of this thread's half that exist
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int t = 32 * hf + i;
-      vv[i] = (rg < D && t < n) ? p.v[((size_t)(t0 + t) * p.h_v + h) * D + rg] : 0.f;
-    }
-    float4 mv[4];
+      for (int i = 0; i < 32; ++i) vv[i] = i < nv ? vp[i * vs] : 0.f;
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mv[j] = *reinterpret_cast<const float4*>(R_ + REC_M + (tid + j * NT) * 4);
-    fGam[tid] = R_[REC_GAM + tid];  // gamma, wend, beta, rk: 4 x 64 consecutive floats
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {  // M (row t, columns s4..s4+3) and its lo part into the M tile
-      const int i4 = tid + j * NT, t = i4 >> 4, s4 = (i4 & 15) * 4;
-      const float4 m = mv[j];
-      *reinterpret_cast<float4*>(sm + L::MT + kf32(t, s4, 128)) = m;
-      *reinterpret_cast<float4*>(sm + L::MT + kf32(64 + t, s4, 128)) =
-          make_float4(tf32_lo(m.x), tf32_lo(m.y), tf32_lo(m.z), tf32_lo(m.w));
+      for (int i = 0; i < 32; ++i) vv[i] = 0.f;  // transition rows: zero values
     }
     if (!mbar_wait(&bar_k[b], (uint32_t)((c >> 1) & 1), kWaitNs)) timed_out = 1;
     k_waited = c;
     // keys: rows past the chunk's end (the next sequence's tokens, or the fill) cleared; lo parts
     // into rows 64-127; K^T and K_lo^T (row k, token t) for the state update.  Warp w, step i:
     // columns 4 (w + 8 i) + [0, 4) of tokens lane and lane + 32 (a warp's K^T stores fill whole
-    // 128-byte rows).
+    // 128-byte rows; every access of the loop takes the fewest shared-memory wavefronts).
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int kc = warp + 8 * i;
@@ -305,6 +317,8 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
       mma_commit(bar_mma);
     }
     __syncwarp();
+    // while the state update runs: the next chunk's M into the M tile (its reader, D2, is done)
+    if (c + 1 < n_chunks) fac_next = load_rec(c + 1);
     wait_mma();
     // X <- gamma_C X + D3, and X, X_lo into TMEM for the next chunk
     {
