@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-depth", type=int, default=3, help="streams and buffer sets in the host-buffer pipeline")
     ap.add_argument("--no-rows", action="store_true", help="skip the varlen / full / chunk-operator / compose rows")
+    ap.add_argument("--case", choices=["compose", "chunk_operator"], default=None,
+                    help="time one secondary workload alone (16 x 2048 fp32 chunks, 32 heads) and exit; "
+                         "the short command the kernel profiles are taken with")
     return ap.parse_args()
 
 
@@ -324,7 +327,8 @@ def measure_rows(dev, flush, peaks, replay_us):
     fl = x.total_tokens * x.h_v * (6 * x.d_k * rows_aug + 64 * (6 * x.d_k + 4 * rows_aug))
     rows["chunk_operator"] = {"chunks": K, "chunk_tokens": 2048, "heads": x.h_v, "dtype": "f32", "us": us,
                               "algorithmic_flops": fl, "tflops": fl / (us * 1e-6) / 1e12,
-                              "path": "fp32 inputs; contractions in split tf32 on warp-level mma.sync"}
+                              "path": "fp32 inputs: prep (norms, gates, Gram on warp-level split tf32, (I + A)^-1) "
+                                      "into records, then the augmented-state scan [S; P] on tcgen05 in split tf32"}
     Tl, Sll = [T[j] for j in range(K)], [Sl[j] for j in range(K)]
     SK = torch.empty((x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
     us = _timed_us(lambda: api.gdn_compose(Tl, Sll, None, S_out=SK), flush, 10)
@@ -333,8 +337,22 @@ def measure_rows(dev, flush, peaks, replay_us):
     rows["compose"] = {"K": K, "heads": x.h_v, "d": x.d_k, "us": us, "algorithmic_bytes": by,
                        "gbs": by / (us * 1e-6) / 1e9, "hbm_frac": by / (us * 1e-6) / 1e9 / hbm,
                        "algorithmic_flops": fl,
-                       "path": "tcgen05 tensor cores, split tf32 (fp32 accuracy)" if x.d_k == 128 and x.d_v == 128
+                       "path": "operators in one array: tensor copies multicast over a 4-CTA cluster per head, "
+                               "tcgen05 split tf32 (fp32 accuracy)" if x.d_k == 128 and x.d_v == 128
                        else "fp32 CUDA cores"}
+    # the same composition with the operators at no common stride (the row-copy kernel)
+    big = torch.empty((K + 2,) + tuple(T.shape[1:]), dtype=torch.float32, device=dev)
+    slots = [K - j + (1 if j == 0 else 0) for j in range(K)]  # reversed, the first a slot further out
+    for j in range(K):
+        big[slots[j]].copy_(T[j])
+    Tsc = [big[slots[j]] for j in range(K)]
+    SK2 = torch.empty_like(SK)
+    us2 = _timed_us(lambda: api.gdn_compose(Tsc, Sll, None, S_out=SK2), flush, 10)
+    torch.cuda.synchronize()
+    rows["compose_scattered"] = {"K": K, "heads": x.h_v, "d": x.d_k, "us": us2, "algorithmic_bytes": by,
+                                 "gbs": by / (us2 * 1e-6) / 1e9, "hbm_frac": by / (us2 * 1e-6) / 1e9 / hbm,
+                                 "path": "operators at no common stride: T rows by bulk copies, tcgen05 split tf32"}
+    del big, Tsc
     api.gdn_get_status()
     rows |= measure_more_rows(dev, flush, peaks, dev_inputs)
     return rows
@@ -766,8 +784,39 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """One secondary workload alone: the chunk operators of 16 isolated 2048-token fp32 chunks
+    (32 heads, d = 128), or their composition (K = 16 operators in one array), each timed over a
+    few calls with the L2 flushed before every call."""
+    import torch
+    from gated_deltanet_state_chunked_gb300 import _lib, api, synthetic
+    _lib.load(build=True)
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    x = synthetic.chunk_workload_inputs()
+    d = {k: torch.from_numpy(np.ascontiguousarray(getattr(x, k))).to(dev) for k in ("k", "v", "g", "beta")}
+    d["cu"] = torch.from_numpy(np.ascontiguousarray(x.cu_seqlens, dtype=np.int32)).to(dev)
+    K = x.n_seqs
+    T = torch.empty((K, x.h_v, x.d_k, x.d_k), dtype=torch.float32, device=dev)
+    Sl = torch.empty((K, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+    op = lambda: api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], d["cu"], T_out=T, Slocal_out=Sl)
+    if args.case == "chunk_operator":
+        us = _timed_us(op, flush, max(args.steps, 1), warmup=max(args.warmup, 1))
+    else:
+        op()
+        SK = torch.empty((x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        Tl, Sll = [T[j] for j in range(K)], [Sl[j] for j in range(K)]
+        us = _timed_us(lambda: api.gdn_compose(Tl, Sll, None, S_out=SK), flush, max(args.steps, 1),
+                       warmup=max(args.warmup, 1))
+    api.gdn_get_status()
+    print(json.dumps({"case": args.case, "us": us, "steps": args.steps, "warmup": args.warmup}))
+
+
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
