@@ -24,6 +24,13 @@
 //   D3 = U^ K^T + U^ K_lo^T + U^_lo K^T            (B = K transposed by the threads: a tf32
 //                                                   operand must be K-major)
 // and the epilogues add the hi*lo halves in fp32.  The state stays in fp32 registers.
+// With bf16 inputs the keys and values are exact in tf32, so the key lo parts vanish: D1 is
+// X K^T + X_lo K^T (N = 64) and D3 U^ K^T + U^_lo K^T; the keys arrive by 16-byte loads into
+// registers during the previous piece's state update instead of by TMA.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
 #include "gdn_internal.cuh"
 #include "tc_common.cuh"
 
@@ -53,7 +60,8 @@ struct COLay {
 };
 
 struct COParams {
-  const float* v;
+  const void* k;  // keys (bf16 inputs; fp32 keys arrive by TMA)
+  const void* v;
   const float* S0;
   const int32_t* cu;
   const float* rec;
@@ -65,7 +73,12 @@ struct COParams {
 
 __device__ __forceinline__ float tf32_lo(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
 
+__device__ __forceinline__ float ld_val(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_val(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+
+template <bool BF16>
 __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant__ CUtensorMap map_k, const COParams p) {
+  using Tin = typename std::conditional<BF16, __nv_bfloat16, float>::type;
   using L = COLay;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -115,8 +128,10 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     mbar_init(&bar_k[0], 1);
     mbar_init(&bar_k[1], 1);
     mbar_fence_init();
-    tma_prefetch_desc(&map_k);
-    if (n_chunks > 0) issue_k(0);
+    if constexpr (!BF16) {
+      tma_prefetch_desc(&map_k);
+      if (n_chunks > 0) issue_k(0);
+    }
   }
   // entering state of this thread's row, columns [64 hf, 64 hf + 64): S0 rows, or identity rows
   float x[64];
@@ -150,7 +165,7 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
 
   int timed_out = 0;
   uint32_t mph = 0;  // phase of bar_mma
-  int k_issued = n_chunks > 0 ? 0 : -1, k_waited = -1;
+  int k_issued = (!BF16 && n_chunks > 0) ? 0 : -1, k_waited = -1;  // key copies (fp32 keys only)
   auto wait_mma = [&]() {
     if (!mbar_wait(bar_mma, mph & 1u, kWaitNs)) timed_out = 1;
     ++mph;
@@ -175,6 +190,22 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     return fac;
   };
   float fac_next = n_chunks > 0 ? load_rec(0) : 0.f;
+  // bf16 keys of piece c: warp w, step j covers the 8 columns 8 ((w + 8 j) & 15) + [0, 8) of token
+  // lane + 32 ((w + 8 j) >> 4) (zero past the piece's end)
+  uint4 kq[4];
+  auto load_k16 = [&](int c) {
+    const int t0c = t_begin + c * C, nc = min(C, t_end - t0c);
+    const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(p.k);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int combo = warp + 8 * j, oct = combo & 15, t = lane + 32 * (combo >> 4);
+      kq[j] = t < nc ? *reinterpret_cast<const uint4*>(kb + ((size_t)(t0c + t) * p.h_k + hk) * D + 8 * oct)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if constexpr (BF16) {
+    if (n_chunks > 0) load_k16(0);
+  }
   const uint64_t dKTT = sdesc_sw128(smem_u32(sm + L::KTT), 16, 1024);
   const uint64_t dMT = sdesc_sw128(smem_u32(sm + L::MT), 16, 1024);
   constexpr uint32_t id128 = idesc_tf32(128, 128);
@@ -182,13 +213,15 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
 
   for (int c = 0; c < n_chunks; ++c) {
     const int t0 = t_begin + c * C, n = min(C, t_end - t0);
-    const int b = c & 1;
+    const int b = BF16 ? 0 : (c & 1);  // (bf16 keys: one buffer, filled by the threads)
     unsigned char* kt = sm + L::KT + b * L::KTBUF;
     // the next chunk's raw keys into the other buffer (its last readers, chunk c - 1's D1 and
     // transposition, finished before that chunk's state update)
     if (tid == 0 && c + 1 < n_chunks) {
-      issue_k(c + 1);
-      k_issued = c + 1;
+      if constexpr (!BF16) {
+        issue_k(c + 1);
+        k_issued = c + 1;
+      }
       // and its M and factors into L2 (read while this chunk's state update runs)
       const float* Rn = p.rec + ((size_t)(first + c + 1) * p.h_v + h) * REC_FLOATS;
       bulk_prefetch_l2(Rn + REC_M, 4096 * 4);
@@ -199,40 +232,60 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     // this chunk's values (row r, tokens [32 hf, +32)): loads in flight while the keys are transposed
     float vv[32];
     if (slice == 0) {
-      const float* vp = p.v + ((size_t)(t0 + 32 * hf) * p.h_v + h) * D + rg;
+      const Tin* vp = static_cast<const Tin*>(p.v) + ((size_t)(t0 + 32 * hf) * p.h_v + h) * D + rg;
       const size_t vs = (size_t)p.h_v * D;
       const int nv = n - 32 * hf;  // tokens of this thread's half that exist
 #pragma unroll
-      for (int i = 0; i < 32; ++i) vv[i] = i < nv ? vp[i * vs] : 0.f;
+      for (int i = 0; i < 32; ++i) vv[i] = i < nv ? ld_val(vp, i * vs) : 0.f;
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) vv[i] = 0.f;  // transition rows: zero values
     }
-    if (!mbar_wait(&bar_k[b], (uint32_t)((c >> 1) & 1), kWaitNs)) timed_out = 1;
-    k_waited = c;
-    // keys: rows past the chunk's end (the next sequence's tokens, or the fill) cleared; lo parts
-    // into rows 64-127; K^T and K_lo^T (row k, token t) for the state update.  Warp w, step i:
-    // columns 4 (w + 8 i) + [0, 4) of tokens lane and lane + 32 (a warp's K^T stores fill whole
-    // 128-byte rows; every access of the loop takes the fewest shared-memory wavefronts).
+    if constexpr (BF16) {
+      // bf16 keys from registers: fp32 rows 0-63 of the key tile and K^T (token lane in each
+      // K^T store: whole 128-byte rows)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int kc = warp + 8 * i;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int t = lane + 32 * hh;
-        float4* src = reinterpret_cast<float4*>(kt + kf32(t, 4 * kc, 128));
-        float4 kv = *src;
-        if (t >= n) {
-          kv = make_float4(0.f, 0.f, 0.f, 0.f);
-          *src = kv;
-        }
-        const float4 lo = make_float4(tf32_lo(kv.x), tf32_lo(kv.y), tf32_lo(kv.z), tf32_lo(kv.w));
-        *reinterpret_cast<float4*>(kt + kf32(64 + t, 4 * kc, 128)) = lo;
-        const float kr[4] = {kv.x, kv.y, kv.z, kv.w}, kl[4] = {lo.x, lo.y, lo.z, lo.w};
+      for (int j = 0; j < 4; ++j) {
+        const int combo = warp + 8 * j, oct = combo & 15, t = lane + 32 * (combo >> 4);
+        const uint32_t w[4] = {kq[j].x, kq[j].y, kq[j].z, kq[j].w};
+        float f[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          *reinterpret_cast<float*>(sm + L::KTT + kf32(4 * kc + e, t, 128)) = kr[e];
-          *reinterpret_cast<float*>(sm + L::KTT + 32768 + kf32(4 * kc + e, t, 128)) = kl[e];
+          f[2 * e] = __uint_as_float(w[e] << 16);
+          f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+        *reinterpret_cast<float4*>(kt + kf32(t, 8 * oct, 128)) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(kt + kf32(t, 8 * oct + 4, 128)) = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(sm + L::KTT + kf32(8 * oct + e, t, 128)) = f[e];
+      }
+    } else {
+      if (!mbar_wait(&bar_k[b], (uint32_t)((c >> 1) & 1), kWaitNs)) timed_out = 1;
+      k_waited = c;
+      // keys: rows past the chunk's end (the next sequence's tokens, or the fill) cleared; lo parts
+      // into rows 64-127; K^T and K_lo^T (row k, token t) for the state update.  Warp w, step i:
+      // columns 4 (w + 8 i) + [0, 4) of tokens lane and lane + 32 (a warp's K^T stores fill whole
+      // 128-byte rows; every access of the loop takes the fewest shared-memory wavefronts).
+  #pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kc = warp + 8 * i;
+  #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int t = lane + 32 * hh;
+          float4* src = reinterpret_cast<float4*>(kt + kf32(t, 4 * kc, 128));
+          float4 kv = *src;
+          if (t >= n) {
+            kv = make_float4(0.f, 0.f, 0.f, 0.f);
+            *src = kv;
+          }
+          const float4 lo = make_float4(tf32_lo(kv.x), tf32_lo(kv.y), tf32_lo(kv.z), tf32_lo(kv.w));
+          *reinterpret_cast<float4*>(kt + kf32(64 + t, 4 * kc, 128)) = lo;
+          const float kr[4] = {kv.x, kv.y, kv.z, kv.w}, kl[4] = {lo.x, lo.y, lo.z, lo.w};
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            *reinterpret_cast<float*>(sm + L::KTT + kf32(4 * kc + e, t, 128)) = kr[e];
+            *reinterpret_cast<float*>(sm + L::KTT + 32768 + kf32(4 * kc + e, t, 128)) = kl[e];
+          }
         }
       }
     }
@@ -247,7 +300,7 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {
         const uint64_t bk = dK + (uint64_t)((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4);
-        mma_tf32_ts(tmem + L::cD1, tmem + L::cX + 8 * kk, bk, id128, kk > 0);
+        mma_tf32_ts(tmem + L::cD1, tmem + L::cX + 8 * kk, bk, BF16 ? id64 : id128, kk > 0);
         mma_tf32_ts(tmem + L::cD1, tmem + L::cXL + 8 * kk, bk, id64, 1);
       }
       mma_commit(bar_mma);
@@ -258,12 +311,12 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     {
       float a[32], bb[32];
       tmem_ld32(tmem + lane_base + L::cD1 + 32 * hf, a);
-      tmem_ld32(tmem + lane_base + L::cD1 + 64 + 32 * hf, bb);
+      if constexpr (!BF16) tmem_ld32(tmem + lane_base + L::cD1 + 64 + 32 * hf, bb);
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int t = 32 * hf + i;
-        const float y = (a[i] + bb[i]) * fRk[t];
+        const float y = (BF16 ? a[i] : a[i] + bb[i]) * fRk[t];
         a[i] = fBeta[t] * (p.scalar_decay ? vv[i] : fmaf(-fGam[t], y, vv[i]));
         bb[i] = tf32_lo(a[i]);
       }
@@ -311,14 +364,17 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
       for (int ts = 0; ts < 8; ++ts) {
         const uint32_t off = (((ts >> 2) * 16384) + (ts & 3) * 32) >> 4;
         mma_tf32_ts(tmem + L::cX, tmem + L::cD2 + 8 * ts, dKTT + off, id128, ts > 0);
-        mma_tf32_ts(tmem + L::cX, tmem + L::cD2 + 8 * ts, dKTT + (32768 >> 4) + off, id128, 1);
+        if constexpr (!BF16) mma_tf32_ts(tmem + L::cX, tmem + L::cD2 + 8 * ts, dKTT + (32768 >> 4) + off, id128, 1);
         mma_tf32_ts(tmem + L::cX, tmem + L::cD2 + 64 + 8 * ts, dKTT + off, id128, 1);
       }
       mma_commit(bar_mma);
     }
     __syncwarp();
     // while the state update runs: the next chunk's M into the M tile (its reader, D2, is done)
-    if (c + 1 < n_chunks) fac_next = load_rec(c + 1);
+    if (c + 1 < n_chunks) {
+      fac_next = load_rec(c + 1);
+      if constexpr (BF16) load_k16(c + 1);  // (its buffer's readers, this piece's D1 and transpose, are done)
+    }
     wait_mma();
     // X <- gamma_C X + D3, and X, X_lo into TMEM for the next chunk
     {
@@ -370,14 +426,17 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
 }  // namespace
 
 bool chunkop_tc_supported(const SimtParams& p, int bf16) {
-  return !bf16 && !p.write_O && p.rec && p.d_k == D && p.d_v == D && p.total_tokens > 0;
+  (void)bf16;
+  return !p.write_O && p.rec && p.d_k == D && p.d_v == D && p.total_tokens > 0;
 }
 
-cudaError_t launch_chunkop_tc(const SimtParams& sp, cudaStream_t stream) {
-  CUtensorMap map;
-  if (!make_map_f32(&map, sp.k, (uint64_t)sp.total_tokens, (uint64_t)sp.h_k * D, kChunk)) return cudaErrorInvalidValue;
+cudaError_t launch_chunkop_tc(const SimtParams& sp, int bf16, cudaStream_t stream) {
+  CUtensorMap map{};  // (bf16 keys are loaded by the threads: no map)
+  if (!bf16 && !make_map_f32(&map, sp.k, (uint64_t)sp.total_tokens, (uint64_t)sp.h_k * D, kChunk))
+    return cudaErrorInvalidValue;
   COParams p{};
-  p.v = static_cast<const float*>(sp.v);
+  p.k = sp.k;
+  p.v = sp.v;
   p.S0 = sp.S0;
   p.cu = sp.cu;
   p.rec = reinterpret_cast<const float*>(sp.rec);
@@ -390,10 +449,11 @@ cudaError_t launch_chunkop_tc(const SimtParams& sp, cudaStream_t stream) {
   p.h_v = sp.h_v;
   p.augmented = sp.augmented;
   p.scalar_decay = sp.scalar_decay;
-  cudaError_t e = cudaFuncSetAttribute(chunkop_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)COLay::ALLOC);
-  if (e != cudaSuccess) return e;
   const dim3 grid(sp.augmented ? 2 : 1, sp.h_v, sp.n_seqs);
-  chunkop_tc_kernel<<<grid, NT, COLay::ALLOC, stream>>>(map, p);
+  auto kern = bf16 ? chunkop_tc_kernel<true> : chunkop_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)COLay::ALLOC);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NT, COLay::ALLOC, stream>>>(map, p);
   return cudaGetLastError();
 }
 

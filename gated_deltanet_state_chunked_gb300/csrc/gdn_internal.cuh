@@ -81,10 +81,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 // The same for a 2D fp32 view: boxes of 32 columns (128 bytes) x box_rows rows.
 bool make_map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
-// Tensor-core state-only scan of the fp32 path (d_k = d_v = 128, fp32 inputs, no outputs), over
-// the records already written into p.rec: the state (augmented or not) in 128-row slices.
+// Tensor-core state-only scan of the fp32 path (d_k = d_v = 128, fp32 or bf16 inputs, no
+// outputs), over the records already written into p.rec: the state (augmented or not) in
+// 128-row slices, at fp32 accuracy.
 bool chunkop_tc_supported(const SimtParams& p, int bf16);
-cudaError_t launch_chunkop_tc(const SimtParams& p, cudaStream_t stream);
+cudaError_t launch_chunkop_tc(const SimtParams& p, int bf16, cudaStream_t stream);
 
 // Sticky status word of the current device (device pointer).
 int* device_status_word();

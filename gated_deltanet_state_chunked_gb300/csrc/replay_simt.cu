@@ -675,8 +675,8 @@ cudaError_t launch_replay_simt_two_pass(SimtParams p, int bf16, void* workspace,
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // state only, fp32, 128-dim heads: the tensor-core scan over the same records
-  if (chunkop_tc_supported(p, bf16)) return launch_chunkop_tc(p, stream);
+  // state only, 128-dim heads: the tensor-core scan over the same records (fp32 accuracy)
+  if (chunkop_tc_supported(p, bf16)) return launch_chunkop_tc(p, bf16, stream);
   return launch_replay_simt(p, bf16, stream);
 }
 

@@ -256,6 +256,36 @@ def test_compose_wait_that_runs_out_reports_timeout_then_recovers(K, layout):
     assert rel_err(host(out), oracle.compose(T, Sl, None)) <= TOL_F32
 
 
+@pytest.mark.parametrize("scalar", [False, True])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_operator_128_dim_heads(dtype, scalar):
+    """128-dim heads: the augmented-state scan on tcgen05 in split tf32 (fp32 and bf16 inputs),
+    ragged sequences (1, 64, 129, 200 tokens), weak gates so that T_C is far from zero."""
+    x = synthetic.make_replay_inputs([200, 1, 64, 129, 3], 2, 4, 128, 128, dtype=dtype, seed=31 + int(scalar),
+                                     gate_scale=1e-3)
+    d = to_device(x)
+    T, Sl = api.gdn_chunk_operator(d["k"], d["g"], d["beta"], d["v"], d["cu_seqlens"], scalar_decay=scalar)
+    torch.cuda.synchronize()
+    api.gdn_get_status()
+    T_ref, Sl_ref = oracle.chunk_operator(x.k, x.g, x.beta, x.v, x.cu_seqlens, scalar_decay=scalar)
+    assert rel_err(host(T), T_ref) <= TOL_F32
+    assert rel_err(host(Sl), Sl_ref) <= TOL_F32
+    for j in range(x.n_seqs):  # every chunk on its own (the 1- and 3-token ones included)
+        assert rel_err(host(T[j]), T_ref[j]) <= TOL_F32
+        assert rel_err(host(Sl[j]), Sl_ref[j]) <= TOL_F32
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_state_only_fp32_accurate_128_dim_heads(dtype):
+    """State-only replay on the fp32-accurate path with 128-dim heads (fp32 inputs, or bf16 with
+    GDN_PRECISE) and an entering state: the same tensor-core scan without the transition rows."""
+    x = synthetic.make_replay_inputs([333, 64, 1, 130], 2, 4, 128, 128, dtype=dtype, seed=33, with_S0=True,
+                                     gate_scale=1e-3)
+    O, S = _run(x, state_only=True, precise=(dtype == "bf16"))
+    S_ref, _ = oracle_replay(x, want_O=False)
+    assert rel_err(host(S), S_ref) <= TOL_F32
+
+
 def test_scalar_decay_family_fp32_and_chunk_operator():
     """The scalar-transition (Mamba-2) family on the fp32 path, and its chunk operator: T_C is
     (prod alpha) I and S_local matches the oracle."""
