@@ -206,6 +206,26 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
   if constexpr (BF16) {
     if (n_chunks > 0) load_k16(0);
   }
+  // values of piece c for this thread's row and tokens [32 hf, +32) (transition rows: zero)
+  auto load_v = [&](int c, float (&out)[32]) {
+    const int t0c = t_begin + c * C, nc = min(C, t_end - t0c);
+    if (slice == 0) {
+      const Tin* vp = static_cast<const Tin*>(p.v) + ((size_t)(t0c + 32 * hf) * p.h_v + h) * D + rg;
+      const size_t vs = (size_t)p.h_v * D;
+      const int nv = nc - 32 * hf;  // tokens of this thread's half that exist
+#pragma unroll
+      for (int i = 0; i < 32; ++i) out[i] = i < nv ? ld_val(vp, i * vs) : 0.f;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) out[i] = 0.f;
+    }
+  };
+  // fp32 inputs: the next piece's values are loaded during the current state update (the loads
+  // then wait on memory while the threads would wait on the MMAs anyway)
+  float vnext[32];
+  if constexpr (!BF16) {
+    if (n_chunks > 0) load_v(0, vnext);
+  }
   const uint64_t dKTT = sdesc_sw128(smem_u32(sm + L::KTT), 16, 1024);
   const uint64_t dMT = sdesc_sw128(smem_u32(sm + L::MT), 16, 1024);
   constexpr uint32_t id128 = idesc_tf32(128, 128);
@@ -229,17 +249,14 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     }
     // this chunk's factors (loaded during the previous state update; their readers are done)
     fGam[tid] = fac_next;
-    // this chunk's values (row r, tokens [32 hf, +32)): loads in flight while the keys are transposed
+    // this chunk's values (row r, tokens [32 hf, +32)): fp32 loaded during the previous state
+    // update; bf16 loaded here, in flight while the keys are transposed
     float vv[32];
-    if (slice == 0) {
-      const Tin* vp = static_cast<const Tin*>(p.v) + ((size_t)(t0 + 32 * hf) * p.h_v + h) * D + rg;
-      const size_t vs = (size_t)p.h_v * D;
-      const int nv = n - 32 * hf;  // tokens of this thread's half that exist
-#pragma unroll
-      for (int i = 0; i < 32; ++i) vv[i] = i < nv ? ld_val(vp, i * vs) : 0.f;
+    if constexpr (BF16) {
+      load_v(c, vv);
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) vv[i] = 0.f;  // transition rows: zero values
+      for (int i = 0; i < 32; ++i) vv[i] = vnext[i];
     }
     if constexpr (BF16) {
       // bf16 keys from registers: fp32 rows 0-63 of the key tile and K^T (token lane in each
@@ -374,6 +391,7 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     if (c + 1 < n_chunks) {
       fac_next = load_rec(c + 1);
       if constexpr (BF16) load_k16(c + 1);  // (its buffer's readers, this piece's D1 and transpose, are done)
+      else load_v(c + 1, vnext);
     }
     wait_mma();
     // X <- gamma_C X + D3, and X, X_lo into TMEM for the next chunk

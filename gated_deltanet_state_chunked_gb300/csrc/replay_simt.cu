@@ -100,22 +100,26 @@ __device__ __forceinline__ void st_out(__nv_bfloat16* p, size_t i, float x) { p[
 
 struct PrepSmem {
   float K[C * KST];
-  float A[C * tcp::MST];
-  float M[C * tcp::MST];
-  float G[C], beta[C], rk[C], rq[C];
+  float A[2][C * tcp::MST];  // per v-head slot
+  float M[2][C * tcp::MST];
+  float G[2][C], beta[2][C], rk[C], rq[C];
   int scratch[20];
   float Q[C * KST];  // last: not allocated when no outputs are wanted
 };
 constexpr size_t kPrepSmemNoQ = offsetof(PrepSmem, Q);
 
-// One CTA per (global chunk, v-head): load and normalise the chunk's keys (and queries), gate
-// sums, the gated Gram matrices A and P, and M = (I + A)^{-1}; write the record.
+// One CTA per (global chunk, key head, pair of its v-heads): load and normalise the chunk's keys
+// (and queries) and form the Gram matrices once; then per v-head slot the gates, A and P, and
+// M = (I + A)^{-1} (one warpgroup per slot); write the records.
 template <typename Tin>
 __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int gc = blockIdx.x, h = blockIdx.y;
+  const int gc = blockIdx.x;
+  const int G_ = p.h_v / p.h_k, npairs = (G_ + 1) / 2;
+  const int hk = blockIdx.y / npairs, pair = blockIdx.y % npairs;
+  const int h0 = hk * G_ + 2 * pair, nslots = min(2, G_ - 2 * pair);  // v-heads h0, h0 + 1
   const int DK = p.d_k;
   int t0, n;
   if (p.cu) {
@@ -128,10 +132,9 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
     t0 = gc * C;
     n = min(C, p.total_tokens - t0);
   }
-  const int hk = h / (p.h_v / p.h_k);
   const Tin* __restrict__ q = static_cast<const Tin*>(p.q);
   const Tin* __restrict__ k = static_cast<const Tin*>(p.k);
-  float* rec = reinterpret_cast<float*>(p.rec) + ((size_t)gc * p.h_v + h) * REC_FLOATS;
+  auto rec_of = [&](int slot) { return reinterpret_cast<float*>(p.rec) + ((size_t)gc * p.h_v + h0 + slot) * REC_FLOATS; };
 
   bool loaded = false;
   if constexpr (sizeof(Tin) == 4) {
@@ -165,13 +168,14 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
       if (p.write_O) sm.Q[t * KST + d] = t < n ? ld_in(q, off) : 0.f;
     }
   }
-  if (tid < C) {
-    const bool in = tid < n;
-    sm.G[tid] = in ? p.g[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
-    sm.beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.h_v + h] : 0.f;
+  if (tid < 2 * C) {  // gates of slot tid / 64
+    const int sl = tid >> 6, t = tid & 63;
+    const bool in = t < n && sl < nslots;
+    sm.G[sl][t] = in ? p.g[(size_t)(t0 + t) * p.h_v + h0 + sl] : 0.f;
+    sm.beta[sl][t] = in ? p.beta[(size_t)(t0 + t) * p.h_v + h0 + sl] : 0.f;
   }
   __syncthreads();
-  // per-token L2 normalisation (q also takes the scale), gate prefix sums
+  // per-token L2 normalisation (q also takes the scale), gate prefix sums (warp 0: slot 0, warp 1: slot 1)
   for (int t = warp; t < C; t += NT / 32) {
     float sk = 0.f, sq = 0.f;
     for (int d = lane; d < DK; d += 32) {
@@ -194,21 +198,22 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
       sm.rq[t] = fq;
     }
   }
-  if (warp == 0) {
-    float a = sm.G[lane], b = sm.G[lane + 32];
+  if (warp < 2) {
+    float a = sm.G[warp][lane], b = sm.G[warp][lane + 32];
     for (int o = 1; o < 32; o <<= 1) {
       const float xa = __shfl_up_sync(0xffffffffu, a, o);
       const float xb = __shfl_up_sync(0xffffffffu, b, o);
       if (lane >= o) { a += xa; b += xb; }
     }
     b += __shfl_sync(0xffffffffu, a, 31);
-    sm.G[lane] = a;
-    sm.G[lane + 32] = b;
+    sm.G[warp][lane] = a;
+    sm.G[warp][lane + 32] = b;
   }
   __syncthreads();
-  {  // Gram matrices on warp-level tensor cores (split tf32): A (strictly lower, gated,
-     // beta-weighted) into shared memory, P into the record (only when outputs are wanted: the
-     // scan reads it for nothing else).  Warp w -> rows 16 (w % 4) + [0, 16), columns 32 (w / 4) + [0, 32).
+  {  // Gram matrices on warp-level tensor cores (split tf32), once for both slots; then per slot A
+     // (strictly lower, gated, beta-weighted) into shared memory and P into the record (only when
+     // outputs are wanted: the scan reads it for nothing else).
+     // Warp w -> rows 16 (w % 4) + [0, 16), columns 32 (w / 4) + [0, 32).
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), g = lane >> 2, q4 = lane & 3;
     float akk[4][4] = {}, aqk[4][4] = {};
     tcp::warp_mma_tf32x3<4>(akk, [&](int m, int kk) { return sm.K[m * KST + kk]; },
@@ -216,38 +221,45 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
     if (p.write_O)
       tcp::warp_mma_tf32x3<4>(aqk, [&](int m, int kk) { return sm.Q[m * KST + kk]; },
                               [&](int kk, int nn) { return sm.K[nn * KST + kk]; }, m0, n0, 0, DK, C);
+    for (int sl = 0; sl < nslots; ++sl) {
+      float* rec = rec_of(sl);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int t = m0 + g + 8 * hh, s0 = n0 + 8 * j + 2 * q4;
-        float pv[2];
+        for (int hh = 0; hh < 2; ++hh) {
+          const int t = m0 + g + 8 * hh, s0 = n0 + 8 * j + 2 * q4;
+          float pv[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int s = s0 + e;
-          const float decay = s <= t ? expf(sm.G[t] - sm.G[s]) : 0.f;
-          sm.A[t * tcp::MST + s] = (s < t && !p.scalar_decay) ? sm.beta[t] * decay * akk[j][2 * hh + e] : 0.f;
-          pv[e] = s <= t ? decay * aqk[j][2 * hh + e] : 0.f;
+          for (int e = 0; e < 2; ++e) {
+            const int s = s0 + e;
+            const float decay = s <= t ? expf(sm.G[sl][t] - sm.G[sl][s]) : 0.f;
+            sm.A[sl][t * tcp::MST + s] =
+                (s < t && !p.scalar_decay) ? sm.beta[sl][t] * decay * akk[j][2 * hh + e] : 0.f;
+            pv[e] = s <= t ? decay * aqk[j][2 * hh + e] : 0.f;
+          }
+          if (p.write_O) *reinterpret_cast<float2*>(rec + REC_P + t * C + s0) = make_float2(pv[0], pv[1]);
         }
-        if (p.write_O) *reinterpret_cast<float2*>(rec + REC_P + t * C + s0) = make_float2(pv[0], pv[1]);
-      }
+    }
   }
   __syncthreads();
-  if (warp < 4) {
-    tcp::invert_unit_lower(sm.A, sm.M, tid, 1);
-  } else if (tid - 128 < C) {
-    const int t = tid - 128;
-    const float Gl = sm.G[C - 1];
-    rec[REC_GAM + t] = expf(sm.G[t]);
-    rec[REC_WEND + t] = expf(Gl - sm.G[t]);
-    rec[REC_BETA + t] = sm.beta[t];
-    rec[REC_RK + t] = sm.rk[t];
-    rec[REC_RQ + t] = sm.rq[t];
-  }
+  const int slot = warp >> 2, gt = tid & 127;  // warpgroup = v-head slot
+  if (slot < nslots) tcp::invert_unit_lower(sm.A[slot], sm.M[slot], gt, 1 + slot);
   __syncthreads();
-  for (int i = tid; i < C * C / 4; i += NT) {
-    const int t = i / (C / 4), s4 = (i % (C / 4)) * 4;
-    *reinterpret_cast<float4*>(rec + REC_M + t * C + s4) = *reinterpret_cast<const float4*>(sm.M + t * tcp::MST + s4);
+  for (int sl = 0; sl < nslots; ++sl) {
+    float* rec = rec_of(sl);
+    if (tid < C) {
+      const int t = tid;
+      const float Gl = sm.G[sl][C - 1];
+      rec[REC_GAM + t] = expf(sm.G[sl][t]);
+      rec[REC_WEND + t] = expf(Gl - sm.G[sl][t]);
+      rec[REC_BETA + t] = sm.beta[sl][t];
+      rec[REC_RK + t] = sm.rk[t];
+      rec[REC_RQ + t] = sm.rq[t];
+    }
+    for (int i = tid; i < C * C / 4; i += NT) {
+      const int t = i / (C / 4), s4 = (i % (C / 4)) * 4;
+      *reinterpret_cast<float4*>(rec + REC_M + t * C + s4) = *reinterpret_cast<const float4*>(sm.M[sl] + t * tcp::MST + s4);
+    }
   }
 }
 
@@ -659,7 +671,8 @@ cudaError_t launch_replay_simt_two_pass(SimtParams p, int bf16, void* workspace,
   p.rec = static_cast<unsigned char*>(workspace);
   const int chunks_ub = tcp::chunks_of(p.total_tokens) + (p.cu ? p.n_seqs : 0);
   if (p.total_tokens > 0) {
-    const dim3 grid(chunks_ub, p.h_v);
+    const int G = p.h_v / p.h_k;
+    const dim3 grid(chunks_ub, p.h_k * ((G + 1) / 2));  // (chunk, key head, pair of its v-heads)
     const size_t smem = p.write_O ? sizeof(PrepSmem) : kPrepSmemNoQ;
     cudaError_t e;
     if (bf16) {
