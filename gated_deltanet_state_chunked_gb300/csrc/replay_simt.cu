@@ -304,11 +304,13 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
     sm.S[r * KST + d] = s;
   }
 
-  // fp32 inputs with 128-dim heads on the record path: each chunk's keys, M, value slice and
-  // gate factors arrive by asynchronous copies issued one chunk (keys) or half a chunk (the
+  // fp32 inputs with 64- or 128-dim heads on the record path: each chunk's keys, M, value slice
+  // and gate factors arrive by asynchronous copies issued one chunk (keys) or half a chunk (the
   // rest) ahead; the keys stay unscaled and their norm factors rk are applied to the products.
+  // A row of keys (queries) is DK / 4 16-byte pieces: thread item i4 -> row i4 >> ksh.
   bool vec = false;
-  if constexpr (sizeof(Tin) == 4) vec = p.rec && (DK == kMaxHead) && (DV % RS == 0);
+  if constexpr (sizeof(Tin) == 4) vec = p.rec && (DK == kMaxHead || DK == kMaxHead / 2) && (DV % RS == 0);
+  const int ksh = DK == kMaxHead ? 5 : 4, kmask = (1 << ksh) - 1, nkj = DK / 16;
   const float* kf = reinterpret_cast<const float*>(k);
   const float* vf = reinterpret_cast<const float*>(v);
   auto rec_of = [&](int ck) {
@@ -317,7 +319,8 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
   auto pf_keys = [&](int t0c, int nc, float* kb) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+      if (j >= nkj) break;
+      const int i4 = tid + j * NT, t = i4 >> ksh, d4 = (i4 & kmask) * 4;
       const bool ok = t < nc;
       cp_async16(kb + t * KST + d4, kf + ((size_t)(t0c + (ok ? t : 0)) * p.h_k + hk) * DK + d4, ok);
     }
@@ -359,15 +362,17 @@ __global__ void __launch_bounds__(NT) simt_chunk_scan_kernel(SimtParams p) {
           float rqv[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
-            qv[j] = t < n ? *reinterpret_cast<const float4*>(qf + ((size_t)(t0 + t) * p.h_k + hk) * DK + d4) : z4;
-            rqv[j] = R[REC_RQ + t];
+            const int i4 = tid + j * NT, t = i4 >> ksh, d4 = (i4 & kmask) * 4;
+            const bool in = j < nkj && t < n;
+            qv[j] = in ? *reinterpret_cast<const float4*>(qf + ((size_t)(t0 + t) * p.h_k + hk) * DK + d4) : z4;
+            rqv[j] = j < nkj ? R[REC_RQ + t] : 0.f;
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) pv[j] = *reinterpret_cast<const float4*>(R + REC_P + (tid + j * NT) * 4);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+            if (j >= nkj) break;
+            const int i4 = tid + j * NT, t = i4 >> ksh, d4 = (i4 & kmask) * 4;
             float* qd = sm.Q + t * KST + d4;
             qd[0] = rqv[j] * qv[j].x; qd[1] = rqv[j] * qv[j].y; qd[2] = rqv[j] * qv[j].z; qd[3] = rqv[j] * qv[j].w;
           }
