@@ -138,21 +138,25 @@ __global__ void __launch_bounds__(NT) simt_chunk_prep_kernel(SimtParams p) {
 
   bool loaded = false;
   if constexpr (sizeof(Tin) == 4) {
-    if (DK == kMaxHead) {  // fp32, 128-dim heads: every 16-byte load of the tile issued at once
+    if (DK == kMaxHead || DK == kMaxHead / 2) {  // fp32, 64- or 128-dim heads: every 16-byte load
+                                                 // of the tile issued at once (DK / 4 per row)
+      const int sh = DK == kMaxHead ? 5 : 4, msk = (1 << sh) - 1, nj = DK / 16;
       const float* kf = reinterpret_cast<const float*>(k);
       const float* qf = reinterpret_cast<const float*>(q);
       float4 kv[8], qv[8];
       const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+        const int i4 = tid + j * NT, t = i4 >> sh, d4 = (i4 & msk) * 4;
         const size_t off = ((size_t)(t0 + t) * p.h_k + hk) * DK + d4;
-        kv[j] = t < n ? *reinterpret_cast<const float4*>(kf + off) : z4;
-        qv[j] = (p.write_O && t < n) ? *reinterpret_cast<const float4*>(qf + off) : z4;
+        const bool in = j < nj && t < n;
+        kv[j] = in ? *reinterpret_cast<const float4*>(kf + off) : z4;
+        qv[j] = (p.write_O && in) ? *reinterpret_cast<const float4*>(qf + off) : z4;
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int i4 = tid + j * NT, t = i4 >> 5, d4 = (i4 & 31) * 4;
+        if (j >= nj) break;
+        const int i4 = tid + j * NT, t = i4 >> sh, d4 = (i4 & msk) * 4;
         *reinterpret_cast<float4*>(sm.K + t * KST + d4) = kv[j];
         if (p.write_O) *reinterpret_cast<float4*>(sm.Q + t * KST + d4) = qv[j];
       }
