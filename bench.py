@@ -315,6 +315,24 @@ def measure_rows(dev, flush, peaks, replay_us):
                     "speedup_full_over_replay": full_us / replay_us}
         rows[tag] = ent
         del d, tail
+    # TF32 tensor peak of this GPU (a cuBLAS TF32 matmul, 8192^3, best of 5): the denominator for
+    # the fp32-accurate contractions below, which run as three tf32 products each
+    a32 = torch.randn((8192, 8192), dtype=torch.float32, device=dev)
+    b32 = torch.randn((8192, 8192), dtype=torch.float32, device=dev)
+    prev_tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    tts = []
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a32, b32)
+        e1.record()
+        torch.cuda.synchronize()
+        tts.append(e0.elapsed_time(e1) * 1e-3)
+    torch.backends.cuda.matmul.allow_tf32 = prev_tf32
+    tf32_peak = 2 * 8192 ** 3 / min(tts[1:]) / 1e12
+    del a32, b32
+    rows["tf32_peak"] = {"tflops": tf32_peak, "how": "torch.matmul fp32 8192^3 with TF32 allowed (cuBLAS), best of 5"}
     # chunk operators of 16 x 2048 fp32 chunks and their composition (K = 16, 32 heads, d = 128)
     x = synthetic.chunk_workload_inputs()
     d = dev_inputs(x)
@@ -327,6 +345,7 @@ def measure_rows(dev, flush, peaks, replay_us):
     fl = x.total_tokens * x.h_v * (6 * x.d_k * rows_aug + 64 * (6 * x.d_k + 4 * rows_aug))
     rows["chunk_operator"] = {"chunks": K, "chunk_tokens": 2048, "heads": x.h_v, "dtype": "f32", "us": us,
                               "algorithmic_flops": fl, "tflops": fl / (us * 1e-6) / 1e12,
+                              "frac_of_tf32_peak": fl / (us * 1e-6) / 1e12 / tf32_peak,
                               "path": "fp32 inputs: prep (norms, gates, Gram on warp-level split tf32, (I + A)^-1) "
                                       "into records, then the augmented-state scan [S; P] on tcgen05 in split tf32"}
     Tl, Sll = [T[j] for j in range(K)], [Sl[j] for j in range(K)]
@@ -336,7 +355,7 @@ def measure_rows(dev, flush, peaks, replay_us):
     fl = K * x.h_v * 2 * x.d_v * x.d_k * x.d_k
     rows["compose"] = {"K": K, "heads": x.h_v, "d": x.d_k, "us": us, "algorithmic_bytes": by,
                        "gbs": by / (us * 1e-6) / 1e9, "hbm_frac": by / (us * 1e-6) / 1e9 / hbm,
-                       "algorithmic_flops": fl,
+                       "algorithmic_flops": fl, "frac_of_tf32_peak": fl / (us * 1e-6) / 1e12 / tf32_peak,
                        "path": "operators in one array: tensor copies multicast over a 4-CTA cluster per head, "
                                "tcgen05 split tf32 (fp32 accuracy)" if x.d_k == 128 and x.d_v == 128
                        else "fp32 CUDA cores"}
