@@ -66,7 +66,7 @@ extern "C" {
 /* flags */
 #define GDN_QK_L2NORM 1u   /* normalise q and k per (token, head): x / sqrt(sum x^2 + 1e-6) */
 #define GDN_STATE_ONLY 2u  /* rebuild the state only; O_out may be NULL and is not written */
-#define GDN_PRECISE 4u     /* bf16 inputs: take the fp32 CUDA-core path instead of the tensor-core path */
+#define GDN_PRECISE 4u     /* bf16 inputs: take the fp32-accurate path (as fp32 inputs do) */
 /* Scalar-decay recurrence family (Mamba-2), which "LinearKV: One Cached State
  * Suffices for Position-Independent Caching in Hybrid LLMs" (composition passage)
  * sets beside GDN: the per-token transition is the scalar alpha_t instead of
@@ -105,10 +105,12 @@ typedef struct {
  * inputs with 128-dim heads run on the tcgen05 tensor cores; with several tails
  * their sequential scans start longest first (a small kernel ranks the tails by
  * length on the stream before the chunk kernels).  fp32 inputs,
- * other head sizes and GDN_PRECISE take the fp32 path: fp32 data, its
- * contractions in split tf32 on warp-level tensor cores (about 21 significant
- * bits), in two passes with pool scratch of (ceil(total_tokens / 64) + n_seqs)
- * * h_v * 34048 bytes (gdn_workspace_bytes gives the amount).
+ * other head sizes and GDN_PRECISE take the fp32-accurate path: fp32 data,
+ * every contraction as three tf32 products (about 21 significant bits), in two
+ * passes with pool scratch of (ceil(total_tokens / 64) + n_seqs) * h_v * 34048
+ * bytes (gdn_workspace_bytes gives the amount); its second pass runs on the
+ * tcgen05 tensor cores for state-only calls with 128-dim heads, on warp-level
+ * tensor cores otherwise.
  */
 int gdn_replay(const gdn_dims* dims, const void* q, const void* k, const void* v, const float* g,
                const float* beta, const int32_t* cu_seqlens, const float* S0, void* O_out, float* S_out,
@@ -155,11 +157,14 @@ int gdn_replay_noalloc(const gdn_dims* dims, const void* q, const void* k, const
  *   T_out       fp32 [n_seqs][h_v][d_k][d_k], T_C row-major, so that
  *               S_out = S_in T_C^T + S_local in this ABI's state layout
  *   Slocal_out  fp32 [n_seqs][h_v][d_v][d_k]
- * q is not needed; dims->scale and GDN_STATE_ONLY are ignored.  Computed on
- * the fp32 path (see gdn_replay) whatever the input dtype, in two passes: the chunk-shared
+ * q is not needed; dims->scale and GDN_STATE_ONLY are ignored.  Computed at
+ * fp32 accuracy whatever the input dtype, in two passes: the chunk-shared
  * quantities ((I + A)^{-1}, gates, norms) once per (64-token piece, v-head)
  * into pool scratch of (ceil(total_tokens / 64) + n_seqs) * h_v * 34048 bytes,
- * then the row slices of the augmented state.
+ * then the 128-row slices of the augmented state [S; P] (P seeded with the
+ * identity, fed zero values; P = T_C^T after the chunk).  With d_k = d_v = 128
+ * the second pass runs on the tensor cores (every contraction as three tf32
+ * products); other head sizes take the fp32 CUDA-core path.
  */
 int gdn_chunk_operator(const gdn_dims* dims, const void* k, const float* g, const float* beta, const void* v,
                        const int32_t* cu_seqlens, float* T_out, float* Slocal_out, void* stream);
