@@ -6,6 +6,10 @@
 // form, which in the row-major convention of this library (S_out = S_in T^T + S_local) is the
 // Horner recursion S_j = S_{j-1} T_j^T + S_local_j, j = 1..K.
 //
+// Two kernels: compose_tc_map_kernel (further down) when the T_j sit at one stride in memory,
+// fetching each T_j once per head by tensor copies multicast over a cluster; and the kernel
+// described here, compose_tc_kernel, for any other pointer array.
+//
 // One CTA per (head, 32-row slice of S), sequential over j.  Transposed, one step is
 //   S_j^T (d_k x 32) = T_j (d_k x d_k) S_{j-1}^T + S_local_j^T,
 // a tcgen05 MMA with M = 128 (lane = output d_k index), N = 32 (state rows), K = 128:
