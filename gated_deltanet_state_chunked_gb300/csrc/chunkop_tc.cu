@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     const int t0 = t_begin + c * C, n = min(C, t_end - t0);
     const int b = BF16 ? 0 : (c & 1);  // (bf16 keys: one buffer, filled by the threads)
     unsigned char* kt = sm + L::KT + b * L::KTBUF;
-    // the next chunk's raw keys into the other buffer (its last readers, chunk c - 1's D1 and
-    // transposition, finished before that chunk's state update)
+    // fp32 keys: the next chunk's raw keys into the other buffer (its last readers, chunk c - 1's
+    // D1 and transposition, finished before that chunk's state update)
     if (tid == 0 && c + 1 < n_chunks) {
       if constexpr (!BF16) {
         issue_k(c + 1);
@@ -283,10 +283,10 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
       // into rows 64-127; K^T and K_lo^T (row k, token t) for the state update.  Warp w, step i:
       // columns 4 (w + 8 i) + [0, 4) of tokens lane and lane + 32 (a warp's K^T stores fill whole
       // 128-byte rows; every access of the loop takes the fewest shared-memory wavefronts).
-  #pragma unroll
+#pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int kc = warp + 8 * i;
-  #pragma unroll
+#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int t = lane + 32 * hh;
           float4* src = reinterpret_cast<float4*>(kt + kf32(t, 4 * kc, 128));
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
           const float4 lo = make_float4(tf32_lo(kv.x), tf32_lo(kv.y), tf32_lo(kv.z), tf32_lo(kv.w));
           *reinterpret_cast<float4*>(kt + kf32(64 + t, 4 * kc, 128)) = lo;
           const float kr[4] = {kv.x, kv.y, kv.z, kv.w}, kl[4] = {lo.x, lo.y, lo.z, lo.w};
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 4; ++e) {
             *reinterpret_cast<float*>(sm + L::KTT + kf32(4 * kc + e, t, 128)) = kr[e];
             *reinterpret_cast<float*>(sm + L::KTT + 32768 + kf32(4 * kc + e, t, 128)) = kl[e];
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(NT, 1) chunkop_tc_kernel(const __grid_constant
     // while the state update runs: the next chunk's M into the M tile (its reader, D2, is done)
     if (c + 1 < n_chunks) {
       fac_next = load_rec(c + 1);
-      if constexpr (BF16) load_k16(c + 1);  // (its buffer's readers, this piece's D1 and transpose, are done)
+      if constexpr (BF16) load_k16(c + 1);  // (into registers; they fill the key tile at the next piece's top)
       else load_v(c + 1, vnext);
     }
     wait_mma();
