@@ -278,12 +278,13 @@ __global__ void __launch_bounds__(CTNT, 1) compose_tc_kernel(const ComposeParams
 // top of step j, from L2, where it was prefetched when step j's copies were issued.
 //
 // Warps 0-7 read T, prepare T_lo and run the epilogue; warp 8 issues the MMAs and owns the
-// copies.  Copy protocol: once every thread has read T_s (the barrier before step s - 1's MMAs),
+// copies.  Copy protocol: once every thread has read T_s (the barrier before step s's MMAs),
 // the CTA posts its own expect_tx for step s + 3 and releases buffer s % 3 by arriving on the
 // "free" barrier of that buffer in all four CTAs; it issues its quarter of step s + 3 once its
-// own free barrier has all four arrivals.  Every CTA sees the same four arrivals, so a step is issued by all four or
-// by none, and a CTA that stops early (a bounded wait gave up) completes any step it released
-// before it leaves; a final cluster barrier keeps every CTA alive until its partners are done.
+// own free barrier has all four arrivals.  Every CTA sees the same four arrivals, so a step is
+// issued by all four or by none, and a CTA that stops early (a bounded wait gave up) completes
+// any step it released before it leaves; a final cluster barrier keeps every CTA alive until
+// its partners are done.
 // ---------------------------------------------------------------------------------------------
 constexpr int kComposeCluster = CTD / CTR;  // CTAs of one head
 constexpr int kTBufs = 3;                   // T_j buffers in shared memory
