@@ -81,6 +81,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 // The same for a 2D fp32 view: boxes of 32 columns (128 bytes) x box_rows rows.
 bool make_map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
+// Operator-form state-only scan (bf16 inputs, d_k = d_v = 128, 32-row slices) over the records
+// of the tensor-core prep kernel written with the Z factor (see state_tc.cu).
+struct StateParams {
+  const int32_t* cu;
+  const int32_t* order;  // tails longest first, or null
+  const float* S0;
+  const unsigned char* rec;
+  float* S_out;
+  int* status;
+  int n_seqs, total_tokens, h_k, h_v;
+};
+cudaError_t launch_state_tc(const CUtensorMap& mk, const CUtensorMap& mv, const StateParams& sp, bool overlap_prep,
+                            cudaStream_t stream);
+
 // Tensor-core state-only scan of the fp32 path (d_k = d_v = 128, fp32 or bf16 inputs, no
 // outputs), over the records already written into p.rec: the state (augmented or not) in
 // 128-row slices, at fp32 accuracy.

@@ -77,6 +77,7 @@ struct PrepParams {
   int* status;
   int n_seqs, total_tokens, h_k, h_v, l2norm, write_O;
   int scalar_decay;  // 1: A = 0 (M = I) and W = 0 (no rank-1 projection term)
+  int zform;         // 1: store Z = -diag(rk exp(G_last - G)) Mw in place of Mw (operator-form scan)
   float scale;
 };
 
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
           const float4 m1 = *reinterpret_cast<const float4*>(mmat + t * MST + s + 4);
           const float mb[8] = {m0.x * b0.x, m0.y * b0.y, m0.z * b0.z, m0.w * b0.w,
                                m1.x * b1.x, m1.y * b1.y, m1.z * b1.z, m1.w * b1.w};
+          const float zt = p.zform ? -gFc[t] : 1.f;  // row factor of Z
           __align__(16) uint32_t bh[4], bl[4], wv[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             const float h1 = __uint_as_float(__float_as_uint(mb[e + 1]) & 0xffff0000u);
             bh[e / 2] = bf16x2_trunc(h0, h1);
             bl[e / 2] = bf16x2_trunc(mb[e] - h0, mb[e + 1] - h1);
-            wv[e / 2] = bf16x2_rne(mb[e] * wf[e], mb[e + 1] * wf[e + 1]);
+            wv[e / 2] = bf16x2_rne(mb[e] * wf[e] * zt, mb[e + 1] * wf[e + 1] * zt);
           }
           *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, s, 64)) = *reinterpret_cast<const uint4*>(bh);
           *reinterpret_cast<uint4*>(rec + kRecMB + kbf16(t, 64 + s, 64)) = *reinterpret_cast<const uint4*>(bl);
@@ -439,8 +441,8 @@ struct ScanLay {
   // 32-row slices (the latency case, few problems): every tile a chunk needs is requested a
   // whole chunk ahead (K has three buffers, Q two), M diag(beta) and P are A operands in TMEM
   // (a 64-column region shared by both: Mb in lanes 0-63, P in lanes 64-127; each product's
-  // other 64 rows are results nobody reads), and K^T [U^hi | U^lo] is one product of N = 2R
-  // that reads K^T once.  64-row slices (the throughput case) have no TMEM columns to spare:
+  // other 64 rows are results nobody reads), and K^T [U^hi | U^lo] has N = 2R (K^T read once),
+  // split over two warps by tokens.  64-row slices (the throughput case) have no TMEM columns to spare:
   // Mb and P are read from shared memory, K and Q are copied once the chain has finished the
   // chunk two before (two K buffers, one Q), and K^T U^ runs over K = [tokens; tokens].
   static constexpr bool NARROW = R == 32;
@@ -463,11 +465,13 @@ struct ScanLay {
   // the chunk's tokens in lanes 0-63 (W S0^T, U~) and 64-127 (Q S0^T; P U is aimed there too).
   // U~ and [W;Q] S0^T have one copy per chunk parity: a chunk's outputs are read back while the
   // next chunk's [W;Q] S0^T runs.  P U has one copy: the next P U is issued only after the
-  // outputs have read it.  Each product is issued by one warp (the tensor pipe takes these
-  // small MMAs one after another whichever warps issue them).
+  // outputs have read it.  [W;Q] S0^T and P U are each issued by one warp; with 32-row slices
+  // K^T U^ comes from the two warps that wrote the U^ rows, each over its own 32 tokens.
   static constexpr int ND1 = 1, NPU = 1;
-  // K^T U^: 32-row slices one accumulator of 2R columns ([hi | lo]); 64-row slices R columns
-  static constexpr uint32_t D2COLS = NARROW ? 2 * R : R;
+  // K^T U^: 32-row slices two accumulators of 2R columns ([hi | lo]), one per issuing warp (each
+  // covers the 32 tokens whose U^ rows that warp wrote); 64-row slices one of R columns
+  static constexpr int ND2 = NARROW ? 2 : 1;
+  static constexpr uint32_t D2COLS = NARROW ? 4 * R : R;
   // accumulator a of [W;Q] S0^T for chunk parity b: cD1 + (2 a + b) R; of P U: cPU + a R
   static constexpr uint32_t cWQ = 0, cU = 128, cD1 = 128 + 2 * R, cD2 = cD1 + 2 * R * ND1, cPU = cD2 + D2COLS;
   static constexpr uint32_t cMP = cPU + R * NPU;  // (32-row slices) Mb in lanes 0-63, P in lanes 64-127
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(NT, 1)
   };
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) {  // the MMA barriers count one commit per issuing warp
-      const int n = &bars[i] == bar_d1 ? L::ND1 : &bars[i] == bar_pu ? L::NPU : 1;
+      const int n = &bars[i] == bar_d1 ? L::ND1 : &bars[i] == bar_pu ? L::NPU : &bars[i] == bar_d2 ? L::ND2 : 1;
       mbar_init(&bars[i], n);
     }
     mbar_fence_init();
@@ -723,29 +727,20 @@ __global__ void __launch_bounds__(NT, 1)
         wait(bar_d1, par);
         tc_fence_after();
         const float sc = gate[64 + t];
-#pragma unroll
-        for (int hh = 0; hh < R / 32; ++hh) {  // 32 state rows at a time
-          float ut[32], dw[32], x[32];
-          tmem_ld32(tmem + lane_base + L::cU + par * R + 32 * hh, ut);
-          tmem_ld32(tmem + lane_base + L::cD1 + par * R + 32 * hh, dw);
-          if constexpr (L::ND1 == 2) tmem_ld32(tmem + lane_base + L::cD1 + (2 + par) * R + 32 * hh, x);
+        if constexpr (L::NARROW) {
+          // U^ rows first, then this warp's half of K^T U^ (the K steps of its own 32 tokens, so no
+          // other warp's rows are needed), then U^T for P U while that half runs.
+          float ut[32], dw[32];
+          tmem_ld32(tmem + lane_base + L::cU + par * R, ut);
+          tmem_ld32(tmem + lane_base + L::cD1 + par * R, dw);
           tmem_ld_wait();
-          if constexpr (L::ND1 == 2) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 w = __fadd2_rn(make_float2(dw[i], dw[i + 1]), make_float2(x[i], x[i + 1]));
-              dw[i] = w.x;
-              dw[i + 1] = w.y;
-            }
-          }
           // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
           __align__(16) uint32_t hp[16], lp[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const int r = 32 * hh + i;
             const float u0 = ut[i] - dw[i], u1 = ut[i + 1] - dw[i + 1];
-            *reinterpret_cast<float*>(sm + L::UT + kf32(r, t, R)) = tf32r(u0);
-            *reinterpret_cast<float*>(sm + L::UT + kf32(r + 1, t, R)) = tf32r(u1);
+            ut[i] = u0;
+            ut[i + 1] = u1;
             const float h0 = u0 * sc, h1 = u1 * sc;
             const float t0 = __uint_as_float(__float_as_uint(h0) & 0xffff0000u);
             const float t1 = __uint_as_float(__float_as_uint(h1) & 0xffff0000u);
@@ -753,12 +748,59 @@ __global__ void __launch_bounds__(NT, 1)
             lp[i / 2] = bf16x2_trunc(h0 - t0, h1 - t1);
           }
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            const int r = 32 * hh + i;
-            if constexpr (L::NARROW) {  // N = 2R: hi in MN columns [0, R), lo in [R, 2R); K = 64 tokens
-              *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, t, 64)) = *reinterpret_cast<const uint4*>(hp + i / 2);
-              *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(R + r, t, 64)) = *reinterpret_cast<const uint4*>(lp + i / 2);
-            } else {  // K = 128: hi in token rows 0-63, lo in 64-127
+          for (int i = 0; i < 32; i += 8) {  // N = 2R: hi in MN columns [0, R), lo in [R, 2R); K = 64 tokens
+            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(i, t, 64)) = *reinterpret_cast<const uint4*>(hp + i / 2);
+            *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(R + i, t, 64)) = *reinterpret_cast<const uint4*>(lp + i / 2);
+          }
+          fence_async_smem();
+          __syncwarp();
+          {  // [K^T U^hi | K^T U^lo] over tokens [32 quad, 32 quad + 32): K steps 2 quad, 2 quad + 1
+            const uint64_t dk = dadd(dKmn, kbuf(c) * 16384u + (uint32_t)quad * 4096u);
+            const uint64_t du = dadd(dUHmn, (uint32_t)quad * 4096u);
+            const uint32_t dst = tmem + L::cD2 + (uint32_t)quad * (2 * R);
+            constexpr uint32_t id2 = idesc_bf16(128, 2 * R, true, true);
+            auto d2 = [&](int j, bool first) {
+              if (elect_one()) mma_bf16(dst, dadd(dk, j * 2048), dadd(du, j * 2048), id2, !first);
+            };
+            issue_range<0, 2>(d2);
+            if (elect_one()) mma_commit(bar_d2);
+            __syncwarp();
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) *reinterpret_cast<float*>(sm + L::UT + kf32(i, t, R)) = tf32r(ut[i]);
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < R / 32; ++hh) {  // 32 state rows at a time
+            float ut[32], dw[32], x[32];
+            tmem_ld32(tmem + lane_base + L::cU + par * R + 32 * hh, ut);
+            tmem_ld32(tmem + lane_base + L::cD1 + par * R + 32 * hh, dw);
+            if constexpr (L::ND1 == 2) tmem_ld32(tmem + lane_base + L::cD1 + (2 + par) * R + 32 * hh, x);
+            tmem_ld_wait();
+            if constexpr (L::ND1 == 2) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 w = __fadd2_rn(make_float2(dw[i], dw[i + 1]), make_float2(x[i], x[i + 1]));
+                dw[i] = w.x;
+                dw[i + 1] = w.y;
+              }
+            }
+            // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
+            __align__(16) uint32_t hp[16], lp[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int r = 32 * hh + i;
+              const float u0 = ut[i] - dw[i], u1 = ut[i + 1] - dw[i + 1];
+              *reinterpret_cast<float*>(sm + L::UT + kf32(r, t, R)) = tf32r(u0);
+              *reinterpret_cast<float*>(sm + L::UT + kf32(r + 1, t, R)) = tf32r(u1);
+              const float h0 = u0 * sc, h1 = u1 * sc;
+              const float t0 = __uint_as_float(__float_as_uint(h0) & 0xffff0000u);
+              const float t1 = __uint_as_float(__float_as_uint(h1) & 0xffff0000u);
+              hp[i / 2] = bf16x2_trunc(t0, t1);
+              lp[i / 2] = bf16x2_trunc(h0 - t0, h1 - t1);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {  // K = 128: hi in token rows 0-63, lo in 64-127
+              const int r = 32 * hh + i;
               *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, t, 128)) = *reinterpret_cast<const uint4*>(hp + i / 2);
               *reinterpret_cast<uint4*>(sm + L::UH + mnbf16(r, 64 + t, 128)) = *reinterpret_cast<const uint4*>(lp + i / 2);
             }
@@ -770,24 +812,16 @@ __global__ void __launch_bounds__(NT, 1)
       fence_async_smem();
       tc_fence_before();
       group_sync(1);
-      // K^T U^ (state) from warp 0, P U (outputs, P in rows 64-127) from warps 1 (and 3)
-      if (warp == 0) {
+      // (64-row slices) K^T U^ (state) from warp 0; P U (outputs, P in rows 64-127) from warp 1
+      if (!L::NARROW && warp == 0) {
         tc_fence_after();
         const uint64_t dk = dadd(dKmn, kbuf(c) * 16384u);
-        if constexpr (L::NARROW) {  // [K^T U^hi | K^T U^lo]: N = 2R, four K steps of 16 tokens
-          constexpr uint32_t id2 = idesc_bf16(128, 2 * R, true, true);
-          auto d2 = [&](int j, bool first) {
-            if (elect_one()) mma_bf16(tmem + L::cD2, dadd(dk, j * 2048), dadd(dUHmn, j * 2048), id2, !first);
-          };
-          issue_range<0, 4>(d2);
-        } else {  // [K^T | K^T] [U^hi; U^lo]: K = 128
-          constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
-          auto d2 = [&](int j, bool first) {
-            if (elect_one())
-              mma_bf16(tmem + L::cD2, dadd(dk, (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, !first);
-          };
-          issue_range<0, 8>(d2);
-        }
+        // [K^T | K^T] [U^hi; U^lo]: K = 128
+        constexpr uint32_t id2 = idesc_bf16(128, R, true, true);
+        auto d2 = [&](int j, bool first) {
+          if (elect_one()) mma_bf16(tmem + L::cD2, dadd(dk, (j & 3) * 2048), dadd(dUHmn, j * 2048), id2, !first);
+        };
+        issue_range<0, 8>(d2);
         if (elect_one()) mma_commit(bar_d2);
         __syncwarp();
       } else if ((warp & 1) == 1 && (warp >> 1) < L::NPU && p.write_O) {
@@ -821,15 +855,21 @@ __global__ void __launch_bounds__(NT, 1)
         const float gC = gate[63];
 #pragma unroll
         for (int hh = 0; hh < R / 32; ++hh) {
-          float d2[32], x[32];
+          float d2[32], x[32], y[32], z[32];  // (32-row slices) [hi | lo] of both accumulators
           tmem_ld32(tmem + lane_base + L::cD2 + 32 * hh, d2);
-          if constexpr (L::NARROW) tmem_ld32(tmem + lane_base + L::cD2 + R + 32 * hh, x);
+          if constexpr (L::NARROW) {
+            tmem_ld32(tmem + lane_base + L::cD2 + R, x);
+            tmem_ld32(tmem + lane_base + L::cD2 + 2 * R, y);
+            tmem_ld32(tmem + lane_base + L::cD2 + 3 * R, z);
+          }
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {  // packed pairs (same rounding as the scalar forms)
             const int r = 32 * hh + i;
             float2 d = make_float2(d2[i], d2[i + 1]);
-            if constexpr (L::NARROW) d = __fadd2_rn(d, make_float2(x[i], x[i + 1]));
+            if constexpr (L::NARROW)
+              d = __fadd2_rn(__fadd2_rn(d, make_float2(x[i], x[i + 1])),
+                             __fadd2_rn(make_float2(y[i], y[i + 1]), make_float2(z[i], z[i + 1])));
             const float2 sn = __ffma2_rn(make_float2(gC, gC), make_float2(sreg[r], sreg[r + 1]), d);
             sreg[r] = sn.x;
             sreg[r + 1] = sn.y;
@@ -856,7 +896,6 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
       wait(bar_kq + par, (c >> 1) & 1);
       wait(bar_r1, par);
-      if (c > 0) wait(bar_d1, (c - 1) & 1);  // the previous [W;Q] S0^T has read the [W;Q] columns
       if constexpr (L::NARROW) {
         // Mb (hi | lo, bf16 pairs) into lanes 0-63 of cMP: U~ of the previous chunk has read them
         // (its completion was waited for below); P U may still read these lanes as rows nobody uses.
@@ -880,6 +919,7 @@ __global__ void __launch_bounds__(NT, 1)
         group_sync(2);
       }
       if (warp == 4) {  // W = Mw K into the [W;Q] columns (M=128: rows 64-127 are replaced by Q below)
+        if (c > 0) wait(bar_d1, (c - 1) & 1);  // the previous [W;Q] S0^T has read the [W;Q] columns
         tc_fence_after();
         constexpr uint32_t idW = idesc_bf16(128, 128, false, true);
 #pragma unroll
@@ -1120,6 +1160,9 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
   pp.g = p.g; pp.beta = p.beta; pp.cu = p.cu; pp.rec = rec; pp.status = p.status;
   pp.n_seqs = p.n_seqs; pp.total_tokens = p.total_tokens; pp.h_k = p.h_k; pp.h_v = p.h_v; pp.l2norm = p.l2norm;
   pp.write_O = p.write_O; pp.scale = p.scale; pp.scalar_decay = p.scalar_decay;
+  // State-only calls with 32-row slices take the operator-form scan, which reads Z instead of Mw.
+  const bool state_form = !p.write_O && replay_tc_rows(p.n_seqs, p.h_v) == 32;
+  pp.zform = state_form ? 1 : 0;
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepLay::ALLOC);
   if (e != cudaSuccess) return e;
   const long long items_ub = ((long long)(p.total_tokens + C - 1) / C + p.n_seqs) * p.h_k;
@@ -1138,6 +1181,12 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
     if (e != cudaSuccess) return e;
   }
 
+  if (state_form) {
+    StateParams st;
+    st.cu = p.cu; st.order = order; st.S0 = p.S0; st.rec = rec; st.S_out = p.S_out; st.status = p.status;
+    st.n_seqs = p.n_seqs; st.total_tokens = p.total_tokens; st.h_k = p.h_k; st.h_v = p.h_v;
+    return launch_state_tc(mk, mv, st, overlap, stream);
+  }
   ScanParams sp;
   sp.cu = p.cu; sp.order = order; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
   sp.status = p.status; sp.n_seqs = p.n_seqs; sp.total_tokens = p.total_tokens; sp.h_k = p.h_k; sp.h_v = p.h_v;

@@ -70,7 +70,7 @@ __device__ __forceinline__ uint32_t mnbf16(uint32_t mn, uint32_t k, uint32_t k_r
   return a * k_rows * 128u + k * 128u + ((((c >> 4) ^ (k & 7u))) << 4) + (c & 15u);
 }
 
-// Chunk bookkeeping over the packed sequences, block-wide (256 threads).
+// Chunk bookkeeping over the packed sequences, block-wide (NW warps, the whole CTA).
 // Chunks are numbered globally: sequence s owns ceil(len_s / 64) consecutive
 // numbers.  A range [cu[i], cu[i+1]) counts only when 0 <= cu[i] <= cu[i+1] <=
 // total_tokens and cu[i] is at least every earlier offset (the offsets are
@@ -79,14 +79,17 @@ __device__ __forceinline__ uint32_t mnbf16(uint32_t mn, uint32_t k, uint32_t k_r
 // buffer.  Other ranges count as 0 chunks and are not valid.  Returns the number
 // of chunks before sequence `seq` (*first), whether `seq` is valid, the total,
 // and, when 0 <= gc < total, the sequence holding global chunk gc (*gc_seq) and
-// its index inside it (*gc_idx).  scratch: 20 ints of shared memory.
+// its index inside it (*gc_idx).  scratch: 2 NW + 4 ints of shared memory.
 struct ChunkInfo {
   int first, total, gc_seq, gc_idx;
   bool valid;
 };
 
-__device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
-                                       int* scratch) {
+template <int NW>
+__device__ inline ChunkInfo chunk_info_n(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
+                                         int* scratch) {
+  constexpr int NTH = 32 * NW;  // offsets examined per round
+  constexpr int RS = 2 * NW;    // results: first, gc_seq, gc_idx, valid
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (n_seqs == 1) {  // one sequence: no scan over the offsets
     const int a = cu[0], b = cu[1];
@@ -101,11 +104,11 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
     __syncthreads();
     return r;
   }
-  if (tid == 0) { scratch[16] = 0; scratch[17] = -1; scratch[18] = 0; scratch[19] = 0; }
+  if (tid == 0) { scratch[RS] = 0; scratch[RS + 1] = -1; scratch[RS + 2] = 0; scratch[RS + 3] = 0; }
   __syncthreads();
-  int carry = 0;                // chunks of the ranges before this block of 256
-  int carry_max = cu[0];        // largest offset before this block's ranges
-  for (int base = 0; base < n_seqs; base += 256) {
+  int carry = 0;                // chunks of the ranges before this round's block of offsets
+  int carry_max = cu[0];        // largest offset before this round's ranges
+  for (int base = 0; base < n_seqs; base += NTH) {
     const int i = base + tid;
     int a = 0, b = INT_MIN;
     if (i < n_seqs) { a = cu[i]; b = cu[i + 1]; }
@@ -118,12 +121,12 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
     }
     int excl = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) excl = INT_MIN;
-    if (lane == 31) scratch[8 + warp] = incl;
+    if (lane == 31) scratch[NW + warp] = incl;
     __syncthreads();
     int wmax = INT_MIN, allmax = INT_MIN;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const int m = scratch[8 + w];
+    for (int w = 0; w < NW; ++w) {
+      const int m = scratch[NW + w];
       if (w < warp) wmax = max(wmax, m);
       allmax = max(allmax, m);
     }
@@ -140,26 +143,31 @@ __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_
     __syncthreads();
     int wsum = 0, all = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const int s = scratch[w];
       if (w < warp) wsum += s;
       all += s;
     }
     const int ex = carry + wsum + inc - cnt;
-    if (i < n_seqs && i == seq) { scratch[16] = ex; scratch[19] = ok ? 1 : 0; }
-    if (cnt > 0 && gc >= ex && gc < ex + cnt) { scratch[17] = i; scratch[18] = gc - ex; }
+    if (i < n_seqs && i == seq) { scratch[RS] = ex; scratch[RS + 3] = ok ? 1 : 0; }
+    if (cnt > 0 && gc >= ex && gc < ex + cnt) { scratch[RS + 1] = i; scratch[RS + 2] = gc - ex; }
     carry += all;
     carry_max = max(carry_max, allmax);
     __syncthreads();
   }
   ChunkInfo r;
-  r.first = (seq >= 0 && seq < n_seqs) ? scratch[16] : carry;
-  r.valid = (seq >= 0 && seq < n_seqs) && scratch[19] != 0;
+  r.first = (seq >= 0 && seq < n_seqs) ? scratch[RS] : carry;
+  r.valid = (seq >= 0 && seq < n_seqs) && scratch[RS + 3] != 0;
   r.total = carry;
-  r.gc_seq = scratch[17];
-  r.gc_idx = scratch[18];
+  r.gc_seq = scratch[RS + 1];
+  r.gc_idx = scratch[RS + 2];
   __syncthreads();
   return r;
+}
+// The 256-thread kernels' form (scratch: 20 ints).
+__device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
+                                       int* scratch) {
+  return chunk_info_n<8>(cu, n_seqs, total_tokens, seq, gc, scratch);
 }
 
 // Named barrier over one 128-thread warpgroup (ids 1, 2, ...; 0 is __syncthreads).

@@ -104,7 +104,11 @@ typedef struct {
  * Computation: chunks of 64 tokens, fp32 state carried between chunks.  bf16
  * inputs with 128-dim heads run on the tcgen05 tensor cores; with several tails
  * their sequential scans start longest first (a small kernel ranks the tails by
- * length on the stream before the chunk kernels).  fp32 inputs,
+ * length on the stream before the chunk kernels).  GDN_STATE_ONLY calls of that
+ * kind with few enough (tail, head) pairs to give every 32-row slice of every
+ * state its own SM carry the state through each chunk's d_k x d_k operator,
+ * built ahead of the carry, so that the chunk-to-chunk chain is one product per
+ * chunk; the result is the same state to rounding.  fp32 inputs,
  * other head sizes and GDN_PRECISE take the fp32-accurate path: fp32 data,
  * every contraction as three tf32 products (about 21 significant bits), in two
  * passes with pool scratch of (ceil(total_tokens / 64) + n_seqs) * h_v * 34048

@@ -185,3 +185,48 @@ def test_scalar_decay_family(with_S0, gate_scale):
                                      with_S0=with_S0, gate_scale=gate_scale)
     O, S = _run(x, scalar_decay=True)
     _check(x, O, S, scalar_decay=True)
+
+
+# State-only calls with few problems (32-row slices) take the operator-form scan: the chunk's
+# d_k x d_k operator K^T Z K is built ahead of the chain and the chain holds one product per chunk.
+@pytest.mark.parametrize("with_S0", [False, True])
+def test_state_only_ragged_few_problems(with_S0):
+    x = synthetic.make_replay_inputs(RAGGED, 2, 4, 128, 128, dtype="bf16", seed=330 + with_S0, unit_qk=False,
+                                     with_S0=with_S0)
+    _, S = _run(x, state_only=True)
+    _check(x, None, S, want_O=False)
+
+
+def test_state_only_weak_decay_carry():
+    x = synthetic.make_replay_inputs([1000, 333], 2, 4, 128, 128, dtype="bf16", seed=332, gate_scale=1e-3,
+                                     with_S0=True)
+    _, S = _run(x, state_only=True)
+    _check(x, None, S, want_O=False)
+
+
+def test_state_only_three_v_heads_per_key_head():
+    x = synthetic.make_replay_inputs([130, 64, 5], 1, 3, 128, 128, dtype="bf16", seed=333, with_S0=True)
+    _, S = _run(x, state_only=True)
+    _check(x, None, S, want_O=False)
+
+
+@pytest.mark.parametrize("with_S0", [False, True])
+def test_state_only_scalar_decay_family(with_S0):
+    x = synthetic.make_replay_inputs([300, 64, 1, 129], 2, 4, 128, 128, dtype="bf16", seed=334, with_S0=with_S0)
+    _, S = _run(x, state_only=True, scalar_decay=True)
+    _check(x, None, S, want_O=False, scalar_decay=True)
+
+
+def test_state_only_single_layer_workload():
+    x = synthetic.workload_inputs("layer_r3277")
+    _, S = _run(x, state_only=True)
+    _check(x, None, S, want_O=False)
+
+
+def test_state_only_matches_outputs_path():
+    """The operator-form state equals the state of the call that also writes outputs (another
+    grouping of the same products) to the bf16 bar."""
+    x = synthetic.make_replay_inputs([700, 90], 2, 4, 128, 128, dtype="bf16", seed=335, with_S0=True)
+    _, S1 = _run(x, state_only=True)
+    _, S2 = _run(x)
+    assert rel_err(host(S1), host(S2)) <= TOL_BF16
