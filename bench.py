@@ -49,9 +49,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-depth", type=int, default=3, help="streams and buffer sets in the host-buffer pipeline")
     ap.add_argument("--no-rows", action="store_true", help="skip the varlen / full / chunk-operator / compose rows")
-    ap.add_argument("--case", choices=["compose", "chunk_operator"], default=None,
-                    help="time one secondary workload alone (16 x 2048 fp32 chunks, 32 heads) and exit; "
-                         "the short command the kernel profiles are taken with")
+    ap.add_argument("--case", choices=["compose", "chunk_operator", "state_only"], default=None,
+                    help="time one secondary workload alone and exit (16 x 2048 fp32 chunks at 32 heads, or "
+                         "the 3277-token layer state only); the short command the kernel profiles are taken with")
     return ap.parse_args()
 
 
@@ -805,13 +805,24 @@ def run_ours(args):
 
 def run_case(args):
     """One secondary workload alone: the chunk operators of 16 isolated 2048-token fp32 chunks
-    (32 heads, d = 128), or their composition (K = 16 operators in one array), each timed over a
-    few calls with the L2 flushed before every call."""
+    (32 heads, d = 128), their composition (K = 16 operators in one array), or the 3277-token
+    layer replayed state only, each timed over a few calls with the L2 flushed before every call."""
     import torch
     from gated_deltanet_state_chunked_gb300 import _lib, api, synthetic
     _lib.load(build=True)
     dev = torch.device("cuda", 0)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if args.case == "state_only":
+        x = make_inputs("layer_r3277")
+        f = lambda a, t: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(t)  # noqa: E731
+        d = dict(q=f(x.q, torch.bfloat16), k=f(x.k, torch.bfloat16), v=f(x.v, torch.bfloat16),
+                 g=f(x.g, torch.float32), beta=f(x.beta, torch.float32), cu=f(x.cu_seqlens, torch.int32))
+        S = torch.empty((x.n_seqs, x.h_v, x.d_v, x.d_k), dtype=torch.float32, device=dev)
+        rep = lambda: api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], S_out=S, state_only=True)
+        us = _timed_us(rep, flush, max(args.steps, 1), warmup=max(args.warmup, 1))
+        api.gdn_get_status()
+        print(json.dumps({"case": args.case, "us": us, "steps": args.steps, "warmup": args.warmup}))
+        return
     x = synthetic.chunk_workload_inputs()
     d = {k: torch.from_numpy(np.ascontiguousarray(getattr(x, k))).to(dev) for k in ("k", "v", "g", "beta")}
     d["cu"] = torch.from_numpy(np.ascontiguousarray(x.cu_seqlens, dtype=np.int32)).to(dev)
