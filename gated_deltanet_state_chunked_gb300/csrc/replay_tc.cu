@@ -18,17 +18,23 @@
 //    merges on warp-level tensor cores), written with beta, G and rk to a per-(chunk, v-head)
 //    record in scratch memory.
 //  * tail_order_kernel -- with several tails, their order longest first.
+//  * chunk_plan_kernel -- with several tails, each tail's first chunk number and whether its
+//    range is valid (one CTA), looked up by the prep items and the scan CTAs.
 //  * chunk_scan_kernel -- one CTA per 32- or 64-row slice of d_v of one (tail, v-head)
 //    state, walking the tail's chunks (R = 32 while all slices fit on the GPU at once, else
 //    64).  Per chunk:
 //      W = Mw K           bf16 (computed factor rounded once)            M=128 N=128 K=64
 //      [Mb_hi|Mb_lo][V;V] bf16 hi/lo split of the computed factor        M=128 N=R   K=128
-//      [W;Q] S0^T         tf32, [W;Q] from TMEM (W and S0 rounded to     M=128 N=R   K=128
-//                         nearest, Q exact)
-//      [K^T|K^T][U^hi;U^lo] bf16 split of the scaled U                   M=128 N=R   K=128
+//      [W;Q] S0^T         tf32, [W;Q] from TMEM (W truncated to tf32     M=128 N=R   K=128
+//                         by the read, S0 rounded to nearest, Q exact)
+//      K^T U^             bf16 split of the scaled U: with 32-row slices
+//                         [K^T U^hi | K^T U^lo], two warps over 32 tokens  M=128 N=2R  K=32 each;
+//                         with 64-row slices [K^T|K^T][U^hi;U^lo]         M=128 N=R   K=128
 //      P U                tf32                                           M=128 N=R   K=64
 //    (the M=128 shapes with 64 meaningful rows put them where the epilogue needs them)
 //    all accumulated in fp32 in TMEM; the state slice stays in fp32 registers.
+// State-only calls with 32-row slices take the operator-form scan of state_tc.cu instead; the
+// prep kernel then stores Z = -diag(rk exp(G_last - G)) Mw in Mw's place.
 // Padded tokens past a tail's end get beta = g = 0 (identity transitions).
 #include <cuda.h>
 #include <cuda_bf16.h>
