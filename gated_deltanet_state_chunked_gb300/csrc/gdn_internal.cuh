@@ -86,7 +86,6 @@ bool make_map_f32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 struct StateParams {
   const int32_t* cu;
   const int32_t* order;  // tails longest first, or null
-  const int32_t* plan;   // chunk plan of several tails (see chunk_info_n in tc_common.cuh), or null
   const float* S0;
   const unsigned char* rec;
   float* S_out;

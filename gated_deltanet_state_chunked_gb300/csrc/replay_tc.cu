@@ -18,8 +18,6 @@
 //    merges on warp-level tensor cores), written with beta, G and rk to a per-(chunk, v-head)
 //    record in scratch memory.
 //  * tail_order_kernel -- with several tails, their order longest first.
-//  * chunk_plan_kernel -- with several tails, each tail's first chunk number and whether its
-//    range is valid (one CTA), looked up by the prep items and the scan CTAs.
 //  * chunk_scan_kernel -- one CTA per 32- or 64-row slice of d_v of one (tail, v-head)
 //    state, walking the tail's chunks (R = 32 while all slices fit on the GPU at once, else
 //    64).  Per chunk:
@@ -79,7 +77,6 @@ struct PrepParams {
   const float* g;
   const float* beta;
   const int32_t* cu;
-  const int32_t* plan;  // chunk plan of several tails (see chunk_info_n), or null
   unsigned char* rec;  // records [chunk][h_v]
   int* status;
   int n_seqs, total_tokens, h_k, h_v, l2norm, write_O;
@@ -128,12 +125,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     bool ok;
   };
   int total = 0;
-  auto item_at = [&](int item) {  // uniform (without a plan chunk_info synchronises the CTA)
+  auto item_at = [&](int item) {  // block-wide (chunk_info synchronises the CTA)
     Item r;
     r.gc = item / p.h_k;
     r.hk = item - r.gc * p.h_k;
-    const ChunkInfo ci = p.plan ? plan_chunk(p.plan, p.n_seqs, r.gc)
-                                : chunk_info(p.cu, p.n_seqs, p.total_tokens, -1, r.gc, scratch);
+    const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, -1, r.gc, scratch);
     total = ci.total;
     r.ok = r.gc < ci.total && ci.gc_seq >= 0;
     r.t0 = r.ok ? p.cu[ci.gc_seq] + ci.gc_idx * C : 0;
@@ -494,7 +490,6 @@ struct ScanLay {
 struct ScanParams {
   const int32_t* cu;
   const int32_t* order;  // tails longest first (scan CTA z takes tail order[z]), or null
-  const int32_t* plan;   // chunk plan of several tails (see chunk_info_n), or null
   const float* S0;
   const unsigned char* rec;
   __nv_bfloat16* O;
@@ -577,7 +572,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int hk = h / (p.h_v / p.h_k);
 
   // A malformed range (see chunk_info) has no records: report it before forming any address.
-  const ChunkInfo ci = p.plan ? plan_seq(p.plan, p.n_seqs, seq) : chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
+  const ChunkInfo ci = chunk_info(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
   if (!ci.valid) {
     if (tid == 0) atomicExch(p.status, GDN_ERR_SHAPE);
     return;
@@ -1140,20 +1135,10 @@ __global__ void tail_order_kernel(const int32_t* __restrict__ cu, int n, int32_t
   }
   order[rank] = i;
 }
-
-// The chunk plan of several tails (one CTA): every tail's first chunk number, the total and each
-// range's validity, so that the prep and scan kernels look a tail or chunk up instead of each
-// CTA scanning the offsets itself.
-__global__ void __launch_bounds__(NT) chunk_plan_kernel(const int32_t* __restrict__ cu, int n, int total_tokens,
-                                                        int32_t* __restrict__ plan) {
-  __shared__ int scratch[20];
-  chunk_info_n<NT / 32>(cu, n, total_tokens, -1, -1, scratch, plan);
-}
 }  // namespace
 
 size_t replay_tc_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
-  // several tails: their order (n ints) and the chunk plan (2 n + 1 ints)
-  return records_bytes(n_seqs, total_tokens, h_v) + (n_seqs > 1 ? (size_t)(3 * n_seqs + 1) * sizeof(int32_t) : 0);
+  return records_bytes(n_seqs, total_tokens, h_v) + (n_seqs > 1 ? (size_t)n_seqs * sizeof(int32_t) : 0);
 }
 
 cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -1166,18 +1151,15 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
     return cudaErrorInvalidValue;
   unsigned char* rec = static_cast<unsigned char*>(workspace);
   int32_t* order = nullptr;
-  int32_t* plan = nullptr;
-  if (p.n_seqs > 1) {  // several tails: longest first, and the chunk plan
+  if (p.n_seqs > 1) {  // several tails: longest first
     order = reinterpret_cast<int32_t*>(rec + records_bytes(p.n_seqs, p.total_tokens, p.h_v));
-    plan = order + p.n_seqs;
     tail_order_kernel<<<(p.n_seqs + 255) / 256, 256, 0, stream>>>(p.cu, p.n_seqs, order);
-    chunk_plan_kernel<<<1, NT, 0, stream>>>(p.cu, p.n_seqs, p.total_tokens, plan);
     const cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
 
   PrepParams pp;
-  pp.g = p.g; pp.beta = p.beta; pp.cu = p.cu; pp.plan = plan; pp.rec = rec; pp.status = p.status;
+  pp.g = p.g; pp.beta = p.beta; pp.cu = p.cu; pp.rec = rec; pp.status = p.status;
   pp.n_seqs = p.n_seqs; pp.total_tokens = p.total_tokens; pp.h_k = p.h_k; pp.h_v = p.h_v; pp.l2norm = p.l2norm;
   pp.write_O = p.write_O; pp.scale = p.scale; pp.scalar_decay = p.scalar_decay;
   // State-only calls with 32-row slices take the operator-form scan, which reads Z instead of Mw.
@@ -1203,12 +1185,12 @@ cudaError_t launch_replay_tc(const SimtParams& p, void* workspace, size_t worksp
 
   if (state_form) {
     StateParams st;
-    st.cu = p.cu; st.order = order; st.plan = plan; st.S0 = p.S0; st.rec = rec; st.S_out = p.S_out; st.status = p.status;
+    st.cu = p.cu; st.order = order; st.S0 = p.S0; st.rec = rec; st.S_out = p.S_out; st.status = p.status;
     st.n_seqs = p.n_seqs; st.total_tokens = p.total_tokens; st.h_k = p.h_k; st.h_v = p.h_v;
     return launch_state_tc(mk, mv, st, overlap, stream);
   }
   ScanParams sp;
-  sp.cu = p.cu; sp.order = order; sp.plan = plan; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
+  sp.cu = p.cu; sp.order = order; sp.S0 = p.S0; sp.rec = rec; sp.O = static_cast<__nv_bfloat16*>(p.O); sp.S_out = p.S_out;
   sp.status = p.status; sp.n_seqs = p.n_seqs; sp.total_tokens = p.total_tokens; sp.h_k = p.h_k; sp.h_v = p.h_v;
   sp.write_O = p.write_O;
   return replay_tc_rows(p.n_seqs, p.h_v) == 64 ? launch_scan<64>(mq, mk, mv, sp, overlap, stream)

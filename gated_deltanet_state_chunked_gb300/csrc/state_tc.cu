@@ -117,8 +117,7 @@ __global__ void __launch_bounds__(SNT, 1)
   const int hk = h / (p.h_v / p.h_k);
 
   // A malformed range (see chunk_info) has no records: report it before forming any address.
-  const ChunkInfo ci =
-      p.plan ? plan_seq(p.plan, p.n_seqs, seq) : chunk_info_n<SW>(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
+  const ChunkInfo ci = chunk_info_n<SW>(p.cu, p.n_seqs, p.total_tokens, seq, -1, scratch);
   if (!ci.valid) {
     if (tid == 0) atomicExch(p.status, GDN_ERR_SHAPE);
     return;

@@ -79,10 +79,7 @@ __device__ __forceinline__ uint32_t mnbf16(uint32_t mn, uint32_t k, uint32_t k_r
 // buffer.  Other ranges count as 0 chunks and are not valid.  Returns the number
 // of chunks before sequence `seq` (*first), whether `seq` is valid, the total,
 // and, when 0 <= gc < total, the sequence holding global chunk gc (*gc_seq) and
-// its index inside it (*gc_idx).  scratch: 2 NW + 4 ints of shared memory.  With offsets_out
-// (2 n_seqs + 1 ints, the chunk plan), also writes every sequence's first chunk number to
-// offsets_out[i] (a range that is not valid owns no chunks: its entry equals the next one), the
-// total to offsets_out[n_seqs] and whether the range is valid to offsets_out[n_seqs + 1 + i].
+// its index inside it (*gc_idx).  scratch: 2 NW + 4 ints of shared memory.
 struct ChunkInfo {
   int first, total, gc_seq, gc_idx;
   bool valid;
@@ -90,7 +87,7 @@ struct ChunkInfo {
 
 template <int NW>
 __device__ inline ChunkInfo chunk_info_n(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
-                                         int* scratch, int32_t* offsets_out = nullptr) {
+                                         int* scratch) {
   constexpr int NTH = 32 * NW;  // offsets examined per round
   constexpr int RS = 2 * NW;    // results: first, gc_seq, gc_idx, valid
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -153,16 +150,11 @@ __device__ inline ChunkInfo chunk_info_n(const int32_t* cu, int n_seqs, int tota
     }
     const int ex = carry + wsum + inc - cnt;
     if (i < n_seqs && i == seq) { scratch[RS] = ex; scratch[RS + 3] = ok ? 1 : 0; }
-    if (offsets_out && i < n_seqs) {
-      offsets_out[i] = ex;
-      offsets_out[n_seqs + 1 + i] = ok ? 1 : 0;
-    }
     if (cnt > 0 && gc >= ex && gc < ex + cnt) { scratch[RS + 1] = i; scratch[RS + 2] = gc - ex; }
     carry += all;
     carry_max = max(carry_max, allmax);
     __syncthreads();
   }
-  if (offsets_out && tid == 0) offsets_out[n_seqs] = carry;
   ChunkInfo r;
   r.first = (seq >= 0 && seq < n_seqs) ? scratch[RS] : carry;
   r.valid = (seq >= 0 && seq < n_seqs) && scratch[RS + 3] != 0;
@@ -172,39 +164,6 @@ __device__ inline ChunkInfo chunk_info_n(const int32_t* cu, int n_seqs, int tota
   __syncthreads();
   return r;
 }
-// The chunk plan's answers for one sequence (no block-wide work): its first chunk and validity.
-__device__ inline ChunkInfo plan_seq(const int32_t* plan, int n_seqs, int seq) {
-  ChunkInfo r;
-  r.total = plan[n_seqs];
-  r.valid = seq >= 0 && seq < n_seqs && plan[n_seqs + 1 + seq] != 0;
-  r.first = r.valid ? plan[seq] : r.total;
-  r.gc_seq = -1;
-  r.gc_idx = 0;
-  return r;
-}
-// ... and for one global chunk gc: the sequence owning it (gc_seq, -1 if none) and its index there.
-__device__ inline ChunkInfo plan_chunk(const int32_t* plan, int n_seqs, int gc) {
-  ChunkInfo r;
-  r.total = plan[n_seqs];
-  r.first = 0;
-  r.valid = false;
-  r.gc_seq = -1;
-  r.gc_idx = 0;
-  if (gc >= 0 && gc < r.total) {
-    // the last sequence whose first chunk is <= gc; a range without chunks shares its first
-    // number with the next range, so the search passes over it
-    int lo = 0, hi = n_seqs;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (plan[mid] <= gc) lo = mid;
-      else hi = mid;
-    }
-    r.gc_seq = lo;
-    r.gc_idx = gc - plan[lo];
-  }
-  return r;
-}
-
 // The 256-thread kernels' form (scratch: 20 ints).
 __device__ inline ChunkInfo chunk_info(const int32_t* cu, int n_seqs, int total_tokens, int seq, int gc,
                                        int* scratch) {

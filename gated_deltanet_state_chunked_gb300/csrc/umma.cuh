@@ -124,6 +124,19 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint64_t* bar, uint32
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
 }
 
+// Spinning variant of mbar_wait for waits on the critical path: polls with the non-blocking
+// test (no suspend, so no wake-up delay), checking the time bound every 64 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  if (timeout_ns == 0) return false;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (global_ns() - t0 > timeout_ns) return false;
+  }
+}
 
 // One lane of the (converged) warp is elected: the issue sites of tcgen05.mma run on whole
 // warps so that their operands stay warp-uniform, and only the elected lane issues.
