@@ -141,19 +141,21 @@ def test_rows_outside_sequences_untouched():
     assert rel_err(host(O[:120]), O_ref[:120]) <= TOL_BF16
 
 
-def test_malformed_cu_seqlens_reports_shape_error():
+@pytest.mark.parametrize("state_only", [True, False])  # the operator-form scan / the scan with outputs
+def test_malformed_cu_seqlens_reports_shape_error(state_only):
     x = synthetic.make_replay_inputs([64, 64], 2, 4, 128, 128, dtype="bf16", seed=308)
     d = to_device(x)
     cu = torch.tensor([0, 100, 50], dtype=torch.int32, device="cuda")
     S = torch.full((2, 4, 128, 128), 9.0, device="cuda")
-    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=True)
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=state_only)
     with pytest.raises(_lib.GdnError) as ei:
         api.gdn_get_status()
     assert ei.value.code == _lib.GDN_ERR_SHAPE
     assert torch.all(S[1] == 9.0)
 
 
-def test_overlapping_forward_ranges_report_shape_error():
+@pytest.mark.parametrize("state_only", [True, False])
+def test_overlapping_forward_ranges_report_shape_error(state_only):
     """Offsets that each run forward but go back ([0, T, 0, T]) would hold more chunks than the
     per-chunk buffers: the ranges after the step back are skipped and reported, nothing else."""
     T = 200
@@ -161,7 +163,7 @@ def test_overlapping_forward_ranges_report_shape_error():
     d = to_device(x)
     cu = torch.tensor([0, T, 0, T], dtype=torch.int32, device="cuda")
     S = torch.full((3, 4, 128, 128), 7.0, device="cuda")
-    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=True)
+    api.gdn_replay(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, S_out=S, state_only=state_only)
     with pytest.raises(_lib.GdnError) as ei:
         api.gdn_get_status()
     assert ei.value.code == _lib.GDN_ERR_SHAPE
