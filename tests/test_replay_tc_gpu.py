@@ -232,3 +232,12 @@ def test_state_only_matches_outputs_path():
     _, S1 = _run(x, state_only=True)
     _, S2 = _run(x)
     assert rel_err(host(S1), host(S2)) <= TOL_BF16
+
+
+def test_state_only_many_problems_64_row_slices():
+    """State only with many (tail, head) pairs: the two-product scan on 64-row slices, no outputs."""
+    rng = np.random.Generator(np.random.PCG64(336))
+    lengths = [int(v) for v in rng.integers(0, 300, size=24)]
+    x = synthetic.make_replay_inputs(lengths, 2, 4, 128, 128, dtype="bf16", seed=337, with_S0=True)
+    _, S = _run(x, state_only=True)
+    _check(x, None, S, want_O=False)
