@@ -93,3 +93,29 @@ def test_operator_form_sign_matters():
         Z = +np.diag(sc) @ M @ np.diag(beta[c0:c0 + C] * gam)  # wrong sign
         St = gC * St + K[c0:c0 + C].T @ np.diag(sc) @ Ut + K[c0:c0 + C].T @ Z @ K[c0:c0 + C] @ St
     assert oracle.rel_err(St.T, S_ref) > 1e-3
+
+
+@pytest.mark.parametrize("T,C", [(29, 8), (48, 16)])
+def test_augmented_state_gives_the_chunk_operator(T, C):
+    """The chunk operator as the tensor-core kernel builds it: the same WY step run on the state
+    augmented with d_k rows P, seeded [S; P] = [0; I] and with no value input for the P rows,
+    ends at [S_local; P] where P is the product of the sequence's transitions (stored transposed:
+    composition applies S <- S T^T + S_local)."""
+    d_k, d_v = 6, 5
+    k, v, g, beta, S0 = _inputs(T, d_k, d_v, seed=41 + T)
+    K = k / np.sqrt((k * k).sum(1, keepdims=True) + 1e-6)
+    St = np.zeros((d_k, d_v + d_k))
+    St[:, d_v:] = np.eye(d_k)
+    for c0 in range(0, T, C):
+        n = min(C, T - c0)
+        Kc = np.zeros((C, d_k)); Kc[:n] = K[c0:c0 + n]
+        Vc = np.zeros((C, d_v + d_k)); Vc[:n, :d_v] = v[c0:c0 + n]
+        gc = np.zeros(C); gc[:n] = g[c0:c0 + n]
+        bc = np.zeros(C); bc[:n] = beta[c0:c0 + n]
+        gC, M, Ut, W, sc, gam = _chunk_pieces(Kc, Vc, gc, bc)
+        St = gC * St + Kc.T @ np.diag(sc) @ (Ut - W @ St)
+    S_local, P = St.T[:d_v], St.T[d_v:]
+    T_ref, Sl_ref = oracle.chunk_operator(k[:, None, :], g[:, None], beta[:, None], v[:, None, :], np.array([0, T]))
+    assert oracle.rel_err(S_local, Sl_ref[0, 0]) < 1e-12
+    assert oracle.rel_err(P.T, T_ref[0, 0]) < 1e-12
+    assert oracle.rel_err(S0 @ P + S_local, _oracle_state(k, v, g, beta, S0)) < 1e-12
