@@ -8,8 +8,10 @@ g = log alpha inside the chunk, gamma_t = exp(G_t)) and beta:
   the WY step:       S^T <- gamma_C S^T + K^T diag(sc) (U~ - W S^T)
   the operator step: S^T <- gamma_C S^T + B^T + A^T S^T,
                      A^T = K^T Z K with Z = -diag(sc) M diag(beta gamma),  B^T = K^T diag(sc) U~.
-Tokens past a sequence's end inside its last chunk take beta = g = 0 (identity steps).  The
-chunk size is small here so that several chunks and a ragged tail fit a small problem.
+and the chunk operator (T_C, S_local) as the WY step on the state augmented with d_k rows,
+seeded [0; I].  Tokens past a sequence's end inside its last chunk take beta = g = 0 (identity
+steps).  The chunk size is small here so that several chunks and a ragged tail fit a small
+problem.
 """
 import numpy as np
 import pytest
