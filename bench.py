@@ -505,13 +505,34 @@ def measure_more_rows(dev, flush, peaks, dev_inputs):
         done.record(s_copy)
         s_main.wait_event(done)
 
+    # the host link alone: the same bytes read back, and one copy each way at the same time (two
+    # streams), the rates the end-to-end leg's uploads and read-backs share
+    h_back = torch.empty(kv_bytes, dtype=torch.uint8).pin_memory()
+
+    def read_back():
+        h_back.copy_(d_kv, non_blocking=True)
+
+    def both_ways():
+        ev = torch.cuda.Event()
+        ev.record(s_main)
+        s_copy.wait_event(ev)
+        with torch.cuda.stream(s_copy):
+            h_back.copy_(d_kv, non_blocking=True)
+        d_kv.copy_(h_kv, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_copy)
+        s_main.wait_event(done)
+
     t_copy, t_rep = timed(copy_only), timed(lambda: replay(s_main))
     t_ser, t_ovl = timed(serialised), timed(overlapped)
+    t_back, t_both = timed(read_back), timed(both_ways)
     rows["copy_overlap"] = {"fa_kv_bytes": kv_bytes, "copy_us": t_copy, "replay_us": t_rep,
                             "serialised_us": t_ser, "overlapped_us": t_ovl,
                             "hidden_us": t_copy + t_rep - t_ovl, "h2d_gbs": kv_bytes / (t_copy * 1e-6) / 1e9,
+                            "d2h_gbs": kv_bytes / (t_back * 1e-6) / 1e9,
+                            "both_ways_gbs": 2 * kv_bytes / (t_both * 1e-6) / 1e9,
                             "fa_kv": "one full-attention layer: 32768 tokens x 8 KV heads x 128 x (K, V), bf16, pinned host"}
-    del h_kv, d_kv, d
+    del h_kv, d_kv, d, h_back
 
     # LinearKV's last-block initializer (the last chunk's local state alone) against the exact
     # composition of all chunk operators and against sequential replay of all chunks, on 16
