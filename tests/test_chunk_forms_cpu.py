@@ -8,8 +8,8 @@ g = log alpha inside the chunk, gamma_t = exp(G_t)) and beta:
   the WY step:       S^T <- gamma_C S^T + K^T diag(sc) (U~ - W S^T)
   the operator step: S^T <- gamma_C S^T + B^T + A^T S^T,
                      A^T = K^T Z K with Z = -diag(sc) M diag(beta gamma),  B^T = K^T diag(sc) U~.
-and the chunk operator (T_C, S_local) as the WY step on the state augmented with d_k rows,
-seeded [0; I].  Tokens past a sequence's end inside its last chunk take beta = g = 0 (identity
+the chunk operator (T_C, S_local) as the WY step on the state augmented with d_k rows,
+seeded [0; I], and the scalar-decay family's chunk step (A = 0, M = I, W = 0).  Tokens past a sequence's end inside its last chunk take beta = g = 0 (identity
 steps).  The chunk size is small here so that several chunks and a ragged tail fit a small
 problem.
 """
@@ -121,3 +121,26 @@ def test_augmented_state_gives_the_chunk_operator(T, C):
     assert oracle.rel_err(S_local, Sl_ref[0, 0]) < 1e-12
     assert oracle.rel_err(P.T, T_ref[0, 0]) < 1e-12
     assert oracle.rel_err(S0 @ P + S_local, _oracle_state(k, v, g, beta, S0)) < 1e-12
+
+
+@pytest.mark.parametrize("T,C", [(37, 8), (16, 16)])
+def test_scalar_decay_chunk_form(T, C):
+    """The scalar-transition (Mamba-2) family as the kernels run it: A = 0, M = I and W = 0, so
+    the chunk step is S^T <- gamma_C S^T + K^T diag(sc) diag(beta) V (and the operator A^T = 0)."""
+    d_k, d_v = 6, 5
+    k, v, g, beta, S0 = _inputs(T, d_k, d_v, seed=61 + T)
+    K = k / np.sqrt((k * k).sum(1, keepdims=True) + 1e-6)
+    St = S0.T.copy()
+    for c0 in range(0, T, C):
+        n = min(C, T - c0)
+        Kc = np.zeros((C, d_k)); Kc[:n] = K[c0:c0 + n]
+        Vc = np.zeros((C, d_v)); Vc[:n] = v[c0:c0 + n]
+        gc = np.zeros(C); gc[:n] = g[c0:c0 + n]
+        bc = np.zeros(C); bc[:n] = beta[c0:c0 + n]
+        G = np.cumsum(gc)
+        sc = np.exp(G[-1] - G)
+        St = np.exp(G[-1]) * St + Kc.T @ np.diag(sc * bc) @ Vc
+    q = np.zeros((T, 1, d_k))
+    S_ref, _ = oracle.replay(q, k[:, None, :], v[:, None, :], g[:, None], beta[:, None], np.array([0, T]),
+                             S0[None, None], want_O=False, scalar_decay=True)
+    assert oracle.rel_err(St.T, S_ref[0, 0]) < 1e-12
