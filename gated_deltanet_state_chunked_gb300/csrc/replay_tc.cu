@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
           __align__(16) uint32_t bh[4], bl[4], wv[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            // Mb as bf16 hi + lo, both truncated (|error| < 2^-16 |Mb|); Mw rounded to nearest even
+            // Mb as bf16 hi + lo, both truncated (|error| < 2^-15 |Mb|); Mw rounded to nearest even
             const float h0 = __uint_as_float(__float_as_uint(mb[e]) & 0xffff0000u);
             const float h1 = __uint_as_float(__float_as_uint(mb[e + 1]) & 0xffff0000u);
             bh[e / 2] = bf16x2_trunc(h0, h1);
@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(NT, 1)
           tmem_ld32(tmem + lane_base + L::cU + par * R, ut);
           tmem_ld32(tmem + lane_base + L::cD1 + par * R, dw);
           tmem_ld_wait();
-          // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
+          // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-15 |U^|)
           __align__(16) uint32_t hp[16], lp[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(NT, 1)
                 dw[i + 1] = w.y;
               }
             }
-            // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-16 |U^|)
+            // U^ = sc U as bf16 hi + lo, both truncated (|error| < 2^-15 |U^|)
             __align__(16) uint32_t hp[16], lp[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {

@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(SNT, 1)
     const int t = 32 * (quad & 1) + lane;  // token of this thread's lane (warps 4-5)
     for (int c = 0; c < nch; ++c) {
       const uint32_t s2 = c & 1, s4 = c & 3, p4 = (c >> 2) & 1;
-      // Y(c) -> [Y_hi | Y_lo] (row d_k = this thread's lane), both truncated (|error| < 2^-16 |Y|)
+      // Y(c) -> [Y_hi | Y_lo] (row d_k = this thread's lane), both truncated (|error| < 2^-15 |Y|)
       wait(&bar_y[s2], (c >> 1) & 1);
       if (c >= 2) wait(&bar_a[(c - 2) & 3], ((c - 2) >> 2) & 1);  // A^T(c-2) has read YS slot s2
       tc_fence_after();
